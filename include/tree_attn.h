@@ -1,0 +1,209 @@
+/*
+ * tree_attn.h -- C ABI of the tree-structured decode attention library
+ * (libtreeattn.so, sm_103a).
+ *
+ * What it computes.  A decoding tree holds a KV cache: the root is the
+ * prompt, every other node a span of generated tokens, and each decode query
+ * token sits in some node u (DeFT notes page, "Decoding tree definition").
+ * Query token t sees every token of u's ancestors, root first, then the
+ * first e_t tokens of u itself (DeFT notes page, "Tree attention
+ * definition").  For every q head h the output is scaled dot-product attention
+ * softmax(s * Q K^T) V over those keys (FastTree review page, "核心公式"),
+ * with s = 1/sqrt(d) unless given, and kv head h / (Hq/Hkv) (grouped-query
+ * attention, the kv_head_mapping of the TGI FlashDecoding pull request).
+ * The log-sum-exp lse = ln sum_j exp(s q.k_j) is returned beside it.
+ *
+ * How.  tree_attn_plan() runs on the host: it groups each node's KV with every
+ * query that shares it (DeFT notes page, "KV-Guided Tree Split"), assigns
+ * every edge 0/1 with the greedy heuristic and cost model of the FastTree
+ * review page ("算法1：贪心二元边赋值", "开销模型"), splits long spans to fill
+ * the GPU (FastTree review page, "GPU高效的长上下文分割"), and uploads the
+ * plan.  tree_attn_run() launches a persistent grouped partial-attention
+ * kernel (tensor cores for stacked query rows, CUDA cores for thin groups)
+ * and a log-sum-exp merge of partial results (DeFT notes page,
+ * "Tree-Topology-Aware Global Reduction Strategy").
+ *
+ * Conventions.
+ *   - All index arrays are int32, host memory, read during the call only (the
+ *     plan keeps its own copies).  Variable-length lists use CSR offsets: an
+ *     array of n+1 prefix sums starting at 0 (the cu_seqlen convention of the
+ *     TGI FlashDecoding pull request).
+ *   - Device tensors are caller-owned, contiguous, 16-byte aligned:
+ *       q        bf16 [n_query_tokens][n_q_heads][head_dim]
+ *       k_pages  bf16 [num_pages][n_kv_heads][page_size][head_dim]
+ *       v_pages  bf16 [num_pages][n_kv_heads][page_size][head_dim]
+ *       out      fp32 [n_query_tokens][n_q_heads][head_dim]
+ *       lse      fp32 [n_query_tokens][n_q_heads] (natural log), may be NULL
+ *     Slots of a page past the end of its node are never read into a result
+ *     (they may hold anything, NaN included).
+ *   - A query whose path holds no visible key gets out = 0, lse = -inf.
+ *   - Every call returns a status; nothing is thrown across the ABI.  On
+ *     failure tree_attn_last_error() describes the cause (thread-local).
+ *   - Supported: head_dim in {64, 128}, page_size == 16, n_q_heads a multiple
+ *     of n_kv_heads, n_q_heads / n_kv_heads <= 128.
+ */
+#ifndef TREE_ATTN_H_
+#define TREE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tree_attn_plan_s* tree_attn_plan_t; /* opaque, library-owned */
+
+typedef enum {
+  TA_OK = 0,
+  TA_ERR_INVALID_ARG = 1,    /* null pointer, bad size or count            */
+  TA_ERR_NOT_A_TREE = 2,     /* parent[] is not one rooted tree             */
+  TA_ERR_PAGE_RANGE = 3,     /* page id or page count out of range          */
+  TA_ERR_UNSUPPORTED = 4,    /* head_dim / page_size / head ratio not built */
+  TA_ERR_ALIGNMENT = 5,      /* device pointer not 16-byte aligned          */
+  TA_ERR_CUDA = 6,           /* a CUDA runtime call failed                  */
+  TA_ERR_OOM = 7,            /* device or host allocation failed            */
+  TA_ERR_DEVICE = 8,         /* a kernel reported an error (see below)      */
+  TA_ERR_HOST_ONLY_PLAN = 9, /* run() on a plan made with host_only = 1     */
+  TA_ERR_BUFFER_TOO_SMALL = 10
+} tree_attn_status;
+
+/* Planner and launch options.  A zero field means "default" (in brackets);
+ * a NULL options pointer means all defaults. */
+typedef struct {
+  int64_t gamma;            /* [64] weight of an intermediate result per row
+                               (the cost model's SplitKVCost_R = gamma*nQ*d) */
+  int64_t beta;             /* [0] optional weight of KV duplicated by a join */
+  int32_t ts_q_set[4];      /* [16,64,128] query tile sizes of the cost model;
+                               zero entries end the list                     */
+  int32_t ts_c;             /* [64] context tile size of the cost model      */
+  int32_t mma_min_rows;     /* [4] rows per kv head from which a group runs
+                               on tensor cores; fewer run on CUDA cores      */
+  int32_t split_tokens;     /* [0 = automatic] chunk length for splitting
+                               long spans; < 0 disables splitting            */
+  int32_t min_split_tokens; /* [256] smallest automatic chunk               */
+  int32_t split_waves;      /* [2] automatic split aims at waves x SMs units */
+  int32_t num_sms;          /* [0 = the current device's, else 152]          */
+  int32_t force_path;       /* [0 = by rows] 1 = CUDA cores, 2 = tensor cores */
+  int32_t host_only;        /* [0] 1: plan on the host only (describe/stats),
+                               no device state; run() then fails             */
+  int32_t wait_timeout_us;  /* [2000000] limit of every in-kernel wait; a
+                               wait that runs out makes the kernel record
+                               TA_DEVERR_TIMEOUT and return                   */
+  const int8_t* force_edges;/* [NULL = greedy] per node 0/1 (root ignored):
+                               use this edge assignment instead             */
+} tree_attn_options;
+
+/* Sizes of a plan, for logging and roofline accounting. */
+typedef struct {
+  int32_t n_nodes, n_query_tokens, n_q_heads, n_kv_heads, head_dim;
+  int32_t n_groups;           /* context-query groups                        */
+  int32_t n_groups_mma;       /* of which on tensor cores                    */
+  int32_t n_units;            /* (group, kv head, query tile, chunk) units   */
+  int32_t grid;               /* persistent CTAs launched by run()           */
+  int32_t n_merge_tokens;     /* query tokens with more than one partial     */
+  int64_t n_partials;         /* partial (O, lse) slots per q head           */
+  int64_t chunk_tokens;       /* chunk length chosen by the split            */
+  int64_t group_kv_tokens;    /* sum of group spans (KV read once per unit)  */
+  int64_t unique_kv_tokens;   /* tokens in the tree                          */
+  int64_t visible_pairs;      /* sum over query tokens of visible keys       */
+  int64_t workspace_bytes;    /* partial results, device                     */
+  int64_t metadata_bytes;     /* plan tables, device                         */
+  double plan_ms;             /* host time spent in tree_attn_plan()         */
+} tree_attn_plan_stats;
+
+/* Device-side error codes read by tree_attn_device_status(). */
+enum { TA_DEVERR_NONE = 0, TA_DEVERR_TIMEOUT = 1, TA_DEVERR_BOUNDS = 2 };
+
+/* Fill *o with the defaults spelled out above. */
+void tree_attn_options_init(tree_attn_options* o);
+
+/* Build a plan for one tree and one set of decode queries.
+ *
+ * parent[n_nodes]           parent id, -1 for exactly one root; must form a
+ *                           tree (no cycle, every node reaches the root).
+ * node_kv_len[n_nodes]      KV tokens per node (>= 0); a node holding the KV
+ *                           of its own decode tokens counts them.
+ * node_page_offsets[n_nodes+1], node_pages[...]
+ *                           CSR block table: node v's tokens sit in order in
+ *                           pages node_pages[off[v]..off[v+1]), and
+ *                           off[v+1]-off[v] == ceil(len_v / page_size); every
+ *                           page id in [0, num_pages).
+ * query_node[n_query_tokens]   node of each decode query token.
+ * query_kv_end[n_query_tokens] tokens of its own node the query sees, in
+ *                           [0, len]; NULL = the whole node.
+ * softmax_scale             <= 0 selects 1/sqrt(head_dim).
+ * opts                      NULL = defaults.
+ * *plan_out                 receives the plan; release it with
+ *                           tree_attn_plan_destroy().  Unless host_only, the
+ *                           plan owns device memory on the current device
+ *                           (tables and the partial-result workspace),
+ *                           allocated and filled here (synchronously).
+ * Errors: TA_ERR_INVALID_ARG, TA_ERR_NOT_A_TREE, TA_ERR_PAGE_RANGE,
+ * TA_ERR_UNSUPPORTED, TA_ERR_CUDA, TA_ERR_OOM; *plan_out is then NULL. */
+tree_attn_status tree_attn_plan(
+    const int32_t* parent, int32_t n_nodes, const int32_t* node_kv_len,
+    const int32_t* node_page_offsets, const int32_t* node_pages,
+    int32_t page_size, int32_t num_pages, const int32_t* query_node,
+    const int32_t* query_kv_end, int32_t n_query_tokens, int32_t n_q_heads,
+    int32_t n_kv_heads, int32_t head_dim, float softmax_scale,
+    const tree_attn_options* opts, tree_attn_plan_t* plan_out);
+
+/* Run the attention of a plan on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream).  Asynchronous: no allocation and no host synchronisation.
+ * Device pointers as in the conventions above; q, k_pages, v_pages are read,
+ * out (and lse if non-NULL) written in full.  One plan may be run any number
+ * of times (e.g. once per layer) but by one stream at a time: its workspace
+ * is shared by all runs.  Errors: TA_ERR_INVALID_ARG, TA_ERR_ALIGNMENT,
+ * TA_ERR_HOST_ONLY_PLAN, TA_ERR_CUDA (launch failure). */
+tree_attn_status tree_attn_run(tree_attn_plan_t plan, const void* q,
+                               const void* k_pages, const void* v_pages,
+                               float* out, float* lse, void* stream);
+
+/* Wait for `stream`, then read and clear the plan's device error word.
+ * *code receives a TA_DEVERR_* value; returns TA_ERR_DEVICE if it is not
+ * TA_DEVERR_NONE, TA_ERR_CUDA if the stream reported an error. */
+tree_attn_status tree_attn_device_status(tree_attn_plan_t plan, void* stream,
+                                         int32_t* code);
+
+/* Kernel timing.  With enable = 1, every later tree_attn_run() of this plan
+ * records CUDA events on its stream before and after each of its kernels
+ * (the partial-attention pass and the merge pass); enable = 0 stops it.
+ * Needs a device plan; events are created here.  Errors: TA_ERR_INVALID_ARG,
+ * TA_ERR_HOST_ONLY_PLAN, TA_ERR_CUDA. */
+tree_attn_status tree_attn_profile_enable(tree_attn_plan_t plan, int32_t enable);
+
+/* Device durations of the last profiled run, in milliseconds: waits for its
+ * last event.  *merge_ms is 0 when the run needed no merge pass.  Either
+ * pointer may be NULL.  Errors: TA_ERR_INVALID_ARG (profiling not enabled or
+ * nothing run yet), TA_ERR_CUDA. */
+tree_attn_status tree_attn_profile_read(tree_attn_plan_t plan, float* partial_ms,
+                                        float* merge_ms);
+
+/* Canonical JSON of the plan's decisions: edge assignment, groups (node,
+ * KV chain, span, tokens, visible ends, rows, path, query tiles, chunks),
+ * partial counts per query token and the unit count.  Writes at most cap
+ * bytes including the terminating NUL; *needed (if non-NULL) receives the
+ * full size.  Returns TA_ERR_BUFFER_TOO_SMALL if cap is too small. */
+tree_attn_status tree_attn_plan_describe(tree_attn_plan_t plan, char* buf,
+                                         size_t cap, size_t* needed);
+
+/* Copy the plan's sizes into *stats. */
+tree_attn_status tree_attn_plan_get_stats(tree_attn_plan_t plan,
+                                          tree_attn_plan_stats* stats);
+
+/* Release a plan and its device memory (NULL is ignored).  The caller must
+ * make sure no run() of the plan is still executing on the GPU. */
+void tree_attn_plan_destroy(tree_attn_plan_t plan);
+
+/* Static string naming a status. */
+const char* tree_attn_status_string(tree_attn_status s);
+
+/* Thread-local description of the last failure in this thread ("" if none). */
+const char* tree_attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREE_ATTN_H_ */

@@ -41,12 +41,13 @@ class PlannerOptions:
     ts_c: int = 64                       # context tile size
     mma_min_rows: int = 4                # rows per kv head to use tensor cores
     mma_tile_rows: int = 128             # MMA query tile (M)
-    simt_tile_rows: int = 4              # CUDA-core query tile
+    simt_tile_rows: int = 8              # CUDA-core query tile
     kv_tile_tokens: int = 128            # chunk granularity (tokens)
-    split_tokens: int = 0                # 0 = automatic long-context split
+    split_tokens: int = 0                # 0 = automatic split, < 0 = never
     min_split_tokens: int = 256          # smallest automatic chunk
     split_waves: int = 2                 # automatic split aims at waves x SMs
     num_sms: int = 152                   # SM count the split targets
+    force_path: int = 0                  # 0 by rows, 1 CUDA cores, 2 MMA
     edges: tuple | None = field(default=None)  # force an assignment (tests)
 
 
@@ -229,11 +230,19 @@ def build_plan(parent, node_kv_len, node_page_offsets, node_pages, page_size,
         g["rows"] = len(g["tokens"]) * r
         assert g["rows"] == rows[g["node"]]
         assert g["span"] == L[g["node"]]
-        g["path"] = "mma" if g["rows"] >= o.mma_min_rows else "simt"
+        if o.force_path == 1:
+            g["path"] = "simt"
+        elif o.force_path == 2:
+            g["path"] = "mma"
+        else:
+            g["path"] = "mma" if g["rows"] >= o.mma_min_rows else "simt"
         tile = o.mma_tile_rows if g["path"] == "mma" else o.simt_tile_rows
         g["qtiles"] = _ceil(g["rows"], tile)
     # Long-context split: chunk length in blocks, a multiple of one KV tile.
-    if o.split_tokens > 0:
+    if o.split_tokens < 0:
+        chunk = max([len(g["blocks"]) for g in groups] + [1])
+        chunk = _ceil(chunk, bpt) * bpt
+    elif o.split_tokens > 0:
         chunk = _ceil(_ceil(o.split_tokens, page_size), bpt) * bpt
     else:
         work = sum(len(g["blocks"]) * n_kv_heads * g["qtiles"] for g in groups)

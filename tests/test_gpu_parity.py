@@ -1,0 +1,115 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tree attention as defined on the DeFT notes page ("Tree attention
+definition") with scaled dot-product attention (FastTree review page,
+"核心公式"); bars: max |err| <= 1e-2, mean |err| <= 1e-3 on the fp32 output,
+|err| <= 1e-3 on lse."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from parity_utils import (compare, make_inputs, oracle_on_tokens, run_gpu,
+                          sample_tokens)
+
+pytestmark = pytest.mark.gpu
+
+
+# ----------------------------------------------------------------- the five workloads
+@pytest.mark.parametrize("name,n_sample", [("tiny", 4), ("long", 10), ("wide", 40),
+                                           ("three", 40), ("irreg", 48)])
+def test_workload_parity(name, n_sample):
+    spec = W.CONFIGS[name]()
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, stats = run_gpu(spec, q, k, v)
+    toks = sample_tokens(spec, n_sample, seed=7)
+    if name == "irreg":  # every speculative token of a few leaves
+        toks = sorted(set(toks) | set(range(8)) | set(range(spec.n_queries - 8, spec.n_queries)))
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
+    compare(out, lse, ref, ref_lse, toks)
+
+
+# ----------------------------------------------------------------- random trees
+@pytest.mark.parametrize("seed", range(16))
+def test_random_tree_parity(seed):
+    rng = np.random.default_rng(seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    spec = W.random_tree(seed, n_nodes=int(rng.integers(1, 40)),
+                         max_len=int(rng.choice([20, 100, 700])),
+                         hq=hkv * int(rng.choice([1, 4, 16])), hkv=hkv,
+                         d=int(rng.choice([64, 128])), zero_len_prob=0.1,
+                         max_queries_per_node=int(rng.integers(1, 5)))
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    opts = {}
+    if seed % 3 == 1:
+        opts["split_tokens"] = 128
+    if seed % 4 == 2:
+        opts["mma_min_rows"] = 1
+    out, lse, _ = run_gpu(spec, q, k, v, **opts)
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    compare(out, lse, ref, ref_lse)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("seed", range(4))
+def test_forced_paths_and_random_edges(path, seed):
+    spec = W.random_tree(40 + seed, n_nodes=25, max_len=300, hq=8, hkv=2, d=128,
+                         max_queries_per_node=3)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    rng = np.random.default_rng(seed)
+    edges = rng.integers(0, 2, size=spec.n_nodes).astype(np.int8)
+    out, lse, _ = run_gpu(spec, q, k, v, force_path=path, force_edges=edges,
+                          split_tokens=int(rng.choice([0, 128, 256])))
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    compare(out, lse, ref, ref_lse)
+
+
+# ----------------------------------------------------------------- edge cases
+def test_empty_paths_give_zero_and_neg_inf():
+    spec = W._finish("empty", [-1, 0, 0], [0, 0, 5], [1, 2, 2], [0, 0, 3], 4, 2, 64, seed=1)
+    q, k, v = make_inputs(spec)
+    out, lse, _ = run_gpu(spec, q, k, v)
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    assert (o[:2] == 0).all() and np.isneginf(l[:2]).all()
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, [2])
+    compare(out, lse, ref, ref_lse, [2])
+
+
+def test_no_queries_is_a_no_op():
+    spec = W._finish("noq", [-1, 0], [20, 20], [], [], 4, 4, 64, seed=2)
+    q, k, v = make_inputs(spec)
+    import tree_structured_decode_gb300 as ta
+    with ta.Plan.from_spec(spec) as p:
+        out, lse = p.run(q, k, v)
+        torch.cuda.synchronize()
+        assert out.numel() == 0
+
+
+def test_single_node_many_tokens_ragged():
+    # one node, 16 * 37 + 5 tokens: many KV tiles and a ragged last page
+    spec = W._finish("one", [-1], [597], [0] * 9, list(range(589, 598)), 8, 2, 128, seed=3)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    for opts in ({}, {"split_tokens": 128}, {"force_path": 1}):
+        out, lse, _ = run_gpu(spec, q, k, v, **opts)
+        ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(9)))
+        compare(out, lse, ref, ref_lse)
+
+
+def test_repeated_runs_reuse_the_plan():
+    spec = W.config_tiny()
+    q, k, v = make_inputs(spec)
+    import tree_structured_decode_gb300 as ta
+    with ta.Plan.from_spec(spec) as p:
+        a, la = p.run(q, k, v)
+        b, lb = p.run(q, k, v)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_large_scores_do_not_overflow():
+    spec = W.two_level(300, 3, 40, 4, 2, 128, seed=5)
+    q, k, v = make_inputs(spec)
+    q = (q.float() * 8).to(torch.bfloat16)  # scores of order +-100
+    out, lse, _ = run_gpu(spec, q, k, v)
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    compare(out, lse, ref, ref_lse)

@@ -1,0 +1,98 @@
+"""The native planner (C ABI, host only) against the reference planner.
+
+Every decision must match exactly: the edge assignment (FastTree review page,
+Algorithm 1 and its cost model), the groups of the virtual tree with their KV
+chains, token lists and visible ends (DeFT notes page, "KV-Guided Tree
+Split"), the path and query tiles of each group, the long-span chunks, the
+partial count of every query token and the number of units."""
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import planner as P
+
+ta = pytest.importorskip("tree_structured_decode_gb300")
+
+
+def _native(spec, **opt):
+    opt.setdefault("num_sms", 152)
+    with ta.Plan.from_spec(spec, host_only=1, **opt) as p:
+        return p.describe(), p.stats()
+
+
+def _reference(spec, **opt):
+    o = P.PlannerOptions(num_sms=opt.get("num_sms", 152))
+    for k in ("gamma", "beta", "ts_c", "mma_min_rows", "split_tokens", "min_split_tokens",
+              "split_waves", "force_path"):
+        if k in opt:
+            setattr(o, k, opt[k])
+    if "ts_q_set" in opt:
+        o.ts_q_set = tuple(opt["ts_q_set"])
+    if "force_edges" in opt:
+        o.edges = tuple(int(x) for x in opt["force_edges"])
+    ref = P.build_plan(spec.parent, spec.node_kv_len, spec.node_page_offsets, spec.node_pages,
+                       spec.page_size, spec.query_node, spec.query_kv_end, spec.n_q_heads,
+                       spec.n_kv_heads, spec.head_dim, o)
+    ref.pop("_blocks")
+    return ref
+
+
+def _same(spec, **opt):
+    got, stats = _native(spec, **opt)
+    ref = _reference(spec, **opt)
+    assert got["edges"] == ref["edges"]
+    assert got["chunk_blocks"] == ref["chunk_blocks"]
+    assert len(got["groups"]) == len(ref["groups"])
+    for a, b in zip(got["groups"], ref["groups"]):
+        assert a == b
+    assert got["partials"] == ref["partials"]
+    assert got["units"] == ref["units"]
+    assert stats["n_units"] == ref["units"]
+    assert stats["n_groups"] == len(ref["groups"])
+    return got, stats
+
+
+@pytest.mark.parametrize("name", ["tiny", "long", "wide", "three", "irreg"])
+def test_configs_match_reference(name):
+    spec = W.CONFIGS[name]()
+    got, stats = _same(spec)
+    assert stats["unique_kv_tokens"] == int(spec.node_kv_len.sum())
+
+
+@pytest.mark.parametrize("seed", range(300))
+def test_random_trees_match_reference(seed):
+    rng = np.random.default_rng(seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    spec = W.random_tree(seed, n_nodes=int(rng.integers(1, 60)), max_len=int(rng.integers(1, 700)),
+                         hq=hkv * int(rng.choice([1, 2, 4, 16])), hkv=hkv,
+                         d=int(rng.choice([64, 128])), zero_len_prob=0.1,
+                         max_queries_per_node=int(rng.integers(1, 5)))
+    opt = {}
+    if seed % 3 == 1:
+        opt["gamma"] = int(rng.integers(0, 2000))
+    if seed % 5 == 2:
+        opt["split_tokens"] = int(rng.choice([-1, 16, 100, 300]))
+    if seed % 7 == 3:
+        opt["mma_min_rows"] = int(rng.integers(1, 200))
+    if seed % 11 == 4:
+        opt["ts_q_set"] = [8, 32]
+        opt["beta"] = 3
+    if seed % 13 == 5:
+        opt["force_path"] = int(rng.integers(1, 3))
+    _same(spec, **opt)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_forced_edge_assignments_match_reference(seed):
+    spec = W.random_tree(500 + seed, n_nodes=12, max_len=90, hq=4, hkv=2, d=64,
+                         max_queries_per_node=3)
+    rng = np.random.default_rng(seed)
+    edges = rng.integers(0, 2, size=spec.n_nodes).astype(np.int8)
+    edges[0] = 0
+    _same(spec, force_edges=edges, split_tokens=int(rng.choice([0, 32, 64])))
+
+
+def test_planning_is_fast_on_the_irregular_tree():
+    spec = W.config_irregular()
+    _, stats = _native(spec)
+    assert stats["plan_ms"] < 200.0

@@ -1,0 +1,56 @@
+// Device-side parameter blocks and kernel launchers (host-callable).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "planner.h"
+
+namespace ta {
+
+// Per group-token record: token id, visible end inside the group span, and
+// the partial-result index of chunk 0 (-1: the token's only partial, written
+// straight to the output).
+struct GroupTok {
+  int32_t tok, vis, pbase, pad;
+};
+
+// Per merge item: a query token with >= 2 partials.
+struct MergeItem {
+  int32_t tok, poff, count, pad;
+};
+
+struct AttnParams {
+  const UnitDesc* units;
+  const int2* blocks;        // {page, span_pos * 32 + valid}
+  const GroupTok* gtoks;
+  const int32_t* cta_off;    // persistent schedule
+  const int32_t* cta_units;
+  const uint16_t* q;         // bf16 bits [nq][hq][d]
+  const uint16_t* k;         // bf16 bits [pages][hkv][16][d]
+  const uint16_t* v;
+  float* out;                // [nq][hq][d]
+  float* lse;                // [nq][hq] natural log, or null
+  float* part_o;             // [n_partials][hq][d]
+  float* part_lse;           // [n_partials][hq], log2 units
+  int32_t* err;              // device error word
+  int32_t hq, hkv, gqa, n_units;
+  float scale_log2;          // softmax scale * log2(e)
+  long long wait_timeout_ns;
+};
+
+struct MergeParams {
+  const MergeItem* items;
+  int32_t n_items, hq;
+  const float* part_o;
+  const float* part_lse;
+  float* out;
+  float* lse;
+};
+
+// Launch the partial-attention pass (every unit).  Returns the launch error.
+cudaError_t launch_partial_attention(const AttnParams& p, int d, int grid, cudaStream_t s);
+// Launch the log-sum-exp merge of partial results.
+cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s);
+
+}  // namespace ta

@@ -1,0 +1,105 @@
+// Host planner for tree-structured decode attention.
+//
+// Turns a decoding tree, its block table and its decode queries into the
+// context-query groups, work units and schedule that the kernels execute.
+// Grouping follows the KV-guided split of the DeFT notes page ("KV-Guided
+// Tree Split": each node's KV grouped with every query that shares it); the
+// edge assignment is Algorithm 1 and the cost model of the FastTree review
+// page ("算法1：贪心二元边赋值", "开销模型"); long spans are split as in
+// "GPU高效的长上下文分割" of the same page.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/tree_attn.h"
+
+namespace ta {
+
+constexpr int kPageSize = 16;
+constexpr int kKvTileTokens = 128;                 // one KV tile = 8 pages
+constexpr int kBlocksPerTile = kKvTileTokens / kPageSize;
+constexpr int kMmaTileRows = 128;                  // tcgen05 M
+constexpr int kSimtTileRows = 8;                   // CUDA-core rows per unit
+constexpr int kPathSimt = 0;
+constexpr int kPathMma = 1;
+
+struct Options {
+  int64_t gamma = 64;
+  int64_t beta = 0;
+  std::vector<int32_t> ts_q{16, 64, 128};
+  int32_t ts_c = 64;
+  int32_t mma_min_rows = 4;
+  int32_t split_tokens = 0;
+  int32_t min_split_tokens = 256;
+  int32_t split_waves = 2;
+  int32_t num_sms = 152;
+  int32_t force_path = 0;
+  int32_t host_only = 0;
+  int32_t wait_timeout_us = 2000000;
+  std::vector<int8_t> force_edges;  // empty = greedy
+};
+
+// One work unit as the kernels read it (32 bytes, device POD).
+struct UnitDesc {
+  int32_t tok_off;  // first entry of the group's token list
+  int32_t kvh;      // kv head
+  int32_t row0;     // first row (token-major, head-minor) of this query tile
+  int32_t nrows;    // rows in this tile
+  int32_t blk0;     // first block (absolute index into the block list)
+  int32_t blk1;     // one past the last block
+  int32_t chunk;    // chunk index inside the group (selects the partial slot)
+  int32_t path;     // kPathSimt or kPathMma
+};
+
+struct GroupInfo {
+  int32_t node;
+  int32_t chain_off, chain_len;  // into HostPlan::chain_nodes (root first)
+  int64_t span;                  // KV tokens of the chain
+  int32_t tok_off, ntok;         // into gtok / gvis / gpbase
+  int32_t rows;                  // ntok * gqa
+  int32_t path;
+  int32_t qtiles;
+  int32_t blk_off, nblk;         // into blk_page / blk_meta
+  int32_t chunk_off, nchunks;    // into chunk_lo / chunk_hi (relative blocks)
+};
+
+struct HostPlan {
+  // problem
+  int32_t n_nodes = 0, nq = 0, hq = 0, hkv = 0, d = 0, gqa = 0;
+  int32_t page_size = kPageSize, num_pages = 0;
+  float scale = 0.f;
+  Options opt;
+  // decisions
+  std::vector<int8_t> edge;
+  std::vector<int64_t> L;
+  std::vector<GroupInfo> groups;
+  std::vector<int32_t> chain_nodes;
+  std::vector<int32_t> gtok, gvis, gpbase;
+  std::vector<int32_t> blk_page, blk_meta;   // meta = span_pos * 32 + valid
+  std::vector<int32_t> chunk_lo, chunk_hi;
+  int64_t chunk_blocks = 0;
+  std::vector<int32_t> pcount, poff;          // per query token
+  int64_t n_partials = 0;
+  std::vector<int32_t> merge_tok;             // tokens with >= 2 partials
+  std::vector<UnitDesc> units;
+  std::vector<int32_t> cta_off, cta_units;    // persistent schedule
+  int32_t grid = 0;
+  // sizes
+  int64_t unique_kv_tokens = 0, group_kv_tokens = 0, visible_pairs = 0;
+};
+
+// Validate and plan.  On failure returns the status and fills *err.
+tree_attn_status build_host_plan(
+    const int32_t* parent, int32_t n_nodes, const int32_t* node_kv_len,
+    const int32_t* node_page_offsets, const int32_t* node_pages,
+    int32_t page_size, int32_t num_pages, const int32_t* query_node,
+    const int32_t* query_kv_end, int32_t nq, int32_t hq, int32_t hkv,
+    int32_t d, float scale, const Options& opt, HostPlan* plan,
+    std::string* err);
+
+// Canonical JSON of the decisions (see tree_attn_plan_describe).
+std::string describe_json(const HostPlan& plan);
+
+}  // namespace ta
