@@ -50,6 +50,10 @@ struct MergeParams {
 
 // Launch the partial-attention pass (every unit).  Returns the launch error.
 cudaError_t launch_partial_attention(const AttnParams& p, int d, int grid, cudaStream_t s);
+// Launch the persistent grouped partial-attention kernel (TMA + tcgen05 /
+// CUDA cores), one CTA per schedule entry.
+cudaError_t launch_tree_attention(const AttnParams& p, int d, int grid, int num_pages,
+                                  cudaStream_t s);
 // Launch the log-sum-exp merge of partial results.
 cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s);
 

@@ -3,6 +3,7 @@
 
 #include <chrono>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -270,7 +271,12 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
     e = cudaEventRecord(P->ev[0], s);
     if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord");
   }
-  e = ta::launch_partial_attention(ap, h.d, h.grid, s);
+  static const bool simple = [] {
+    const char* v = std::getenv("TREE_ATTN_SIMPLE_KERNEL");
+    return v && v[0] == '1';
+  }();
+  e = simple ? ta::launch_partial_attention(ap, h.d, h.grid, s)
+             : ta::launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
   if (e != cudaSuccess) return cuda_err(e, "partial attention launch");
   if (P->profiling) {
     e = cudaEventRecord(P->ev[1], s);

@@ -1,0 +1,709 @@
+// Persistent grouped partial-attention kernel for sm_103a.
+//
+// One CTA per SM walks its list of work units (group, kv head, query tile,
+// chunk).  A unit's KV span is streamed once, 128 tokens (8 pages) per tile,
+// by TMA into a ring of shared-memory stages (128-byte swizzle, one box per
+// page and 64-column half).  The tile is consumed on one of two paths:
+//
+//  * tensor cores (stacked query rows; FastTree review page, "高效树结构注意力
+//    内核设计": GEMV becomes GEMM once a group's queries are stacked): the
+//    group's query tile (128 rows = query tokens x GQA heads) sits in shared
+//    memory; S = Q K^T goes to TMEM (double-buffered), the four compute warps
+//    read one row per thread, apply the mask and an online softmax (the
+//    running max is raised only when it grows by more than 2^8, so O is
+//    rarely rescaled), write P as bf16 to shared memory, and tcgen05 adds
+//    P V into the O accumulator in TMEM.
+//  * CUDA cores (thin groups): the compute warps split the tile's pages,
+//    lanes split the head dimension, and each warp keeps its own online
+//    softmax; the warps' states are combined at the end of the unit.
+//
+// Each row's result is written as final output when the row has one partial,
+// else as a normalised partial (O, lse in base 2) for the merge pass (DeFT
+// notes page, "Tree-Topology-Aware Global Reduction Strategy").
+//
+// Roles: warps 0-3 compute (thread i owns TMEM lane / query row i), warp 4
+// issues TMA, warp 5 owns TMEM and issues tcgen05.mma.  Every wait is
+// bounded: if one runs out the CTA records TA_DEVERR_TIMEOUT, stops issuing
+// work, waits (bounded) for its copies and MMAs in flight, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace ta {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kComputeThreads = 128;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kTileTok = 128;
+constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr uint32_t kTmemCols = 512;
+constexpr long long kDrainLimitNs = 200000000;  // 200 ms for copies / MMAs already in flight
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kQBytes = 128 * D * 2;
+  static constexpr int kTileBytes = kTileTok * D * 2;  // K (or V) of one tile
+  static constexpr int kPBytes = 128 * kTileTok * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffP = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kNumBars = 2 * kStages + 9;
+  static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1024-B alignment slack
+  static constexpr uint32_t kBlockBytes = 16 * D * 2;                // one page-head
+  static constexpr uint32_t kIdescQK = ptx::idesc_bf16(128, kTileTok, 0);
+  static constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, D, 1);
+};
+
+struct Shared {
+  uint32_t base;  // 1024-aligned shared address of the layout
+  uint8_t* ptr;
+  volatile uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+
+template <int D>
+struct Bars {
+  uint32_t b;
+  __device__ uint32_t full(int s) const { return b + 8 * s; }
+  __device__ uint32_t empty(int s) const { return b + 8 * (Cfg<D>::kStages + s); }
+  __device__ uint32_t s_full(int i) const { return b + 8 * (2 * Cfg<D>::kStages + i); }
+  __device__ uint32_t s_free(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 2 + i); }
+  __device__ uint32_t p_full() const { return b + 8 * (2 * Cfg<D>::kStages + 4); }
+  __device__ uint32_t p_empty() const { return b + 8 * (2 * Cfg<D>::kStages + 5); }
+  __device__ uint32_t q_full() const { return b + 8 * (2 * Cfg<D>::kStages + 6); }
+  __device__ uint32_t o_full() const { return b + 8 * (2 * Cfg<D>::kStages + 7); }
+  __device__ uint32_t drain() const { return b + 8 * (2 * Cfg<D>::kStages + 8); }
+};
+
+// Bounded wait.  Returns false (and does not wait) once the CTA has aborted;
+// a wait that exceeds the limit aborts the CTA and records the error.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Shared& sh,
+                                         int32_t* err, long long limit_ns) {
+  if (*sh.abort_flag) return false;
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((n & 15) == 0) {
+      if (*sh.abort_flag) return false;
+      if ((long long)(ptx::globaltimer() - t0) > limit_ns) {
+        *sh.abort_flag = 1;
+        atomicCAS(err, 0, TA_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used while draining after an abort: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit_ns) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if ((long long)(ptx::globaltimer() - t0) > limit_ns) return;
+}
+
+__device__ __forceinline__ int unit_tiles(const UnitDesc& u) {
+  return (u.blk1 - u.blk0 + 7) >> 3;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// ============================================================== producer
+template <int D>
+__device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
+                         int u0, int u1, const Shared& sh, const Bars<D>& B) {
+  using C = Cfg<D>;
+  uint32_t g = 0;
+  uint32_t filled[C::kStages];  // 1 + tile index of the last fill issued per stage
+#pragma unroll
+  for (int s = 0; s < C::kStages; ++s) filled[s] = 0;
+  for (int ui = u0; ui < u1; ++ui) {
+    const UnitDesc u = p.units[p.cta_units[ui]];
+    for (int b0 = u.blk0; b0 < u.blk1; b0 += 8, ++g) {
+      const int s = g % C::kStages;
+      if (g >= (uint32_t)C::kStages &&
+          !wait_bar(B.empty(s), ((g / C::kStages) + 1) & 1, sh, p.err, p.wait_timeout_ns))
+        continue;
+      if (*sh.abort_flag) continue;
+      const int nb = min(8, u.blk1 - b0);
+      ptx::mbar_arrive_expect_tx(B.full(s), (uint32_t)nb * 2u * C::kBlockBytes);
+      const uint32_t kdst = sh.base + C::kOffK + s * C::kTileBytes;
+      const uint32_t vdst = sh.base + C::kOffV + s * C::kTileBytes;
+      for (int bb = 0; bb < nb; ++bb) {
+        const int page = p.blocks[b0 + bb].x;
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h) {
+          const uint32_t off = h * (kTileTok * 128) + bb * (16 * 128);
+          ptx::tma_load_4d(kdst + off, tmk, 64 * h, 0, u.kvh, page, B.full(s));
+          ptx::tma_load_4d(vdst + off, tmv, 64 * h, 0, u.kvh, page, B.full(s));
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < C::kStages; ++t)
+        if (t == s) filled[t] = g + 1;
+    }
+  }
+  if (*sh.abort_flag) {
+    // let the last copy issued into every stage land before the CTA exits
+#pragma unroll
+    for (int s = 0; s < C::kStages; ++s)
+      if (filled[s]) drain_wait(B.full(s), ((filled[s] - 1) / C::kStages) & 1, kDrainLimitNs);
+  }
+}
+
+// ============================================================== MMA issuer
+template <int D>
+__device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh,
+                           const Bars<D>& B, uint32_t tmem) {
+  using C = Cfg<D>;
+  uint32_t g = 0, gm = 0, nu = 0;
+  const uint32_t qbase = sh.base + C::kOffQ;
+  const uint32_t pbase = sh.base + C::kOffP;
+  bool issued = false;
+  for (int ui = u0; ui < u1; ++ui) {
+    const UnitDesc u = p.units[p.cta_units[ui]];
+    const int T = unit_tiles(u);
+    if (u.path != kPathMma || T == 0) {
+      g += T;
+      continue;
+    }
+    const bool qok = wait_bar(B.q_full(), nu & 1, sh, p.err, p.wait_timeout_ns);
+    ptx::tc_fence_after();
+    auto issue_pv = [&](int jj) {
+      const bool ok = wait_bar(B.p_full(), (gm + jj) & 1, sh, p.err, p.wait_timeout_ns);
+      ptx::tc_fence_after();
+      const int s = (g + jj) % C::kStages;
+      const int nbk = min(8, u.blk1 - (u.blk0 + 8 * jj));
+      if (ok && !*sh.abort_flag) {
+        const uint32_t vb = sh.base + C::kOffV + s * C::kTileBytes;
+        for (int kk = 0; kk < nbk; ++kk) {
+          const uint64_t ad = ptx::sdesc_sw128(pbase + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(vb + kk * 2048, kTileTok * 128, 1024);
+          ptx::mma_bf16(tmem + 256, ad, bd, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        issued = true;
+      }
+      ptx::mma_commit(B.empty(s));
+      ptx::mma_commit(B.p_empty());
+    };
+    for (int j = 0; j < T; ++j) {
+      const int s = (g + j) % C::kStages;
+      const int sb = (gm + j) & 1;
+      bool ok = qok && wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+      ok = ok && wait_bar(B.s_free(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
+      ptx::tc_fence_after();
+      if (ok && !*sh.abort_flag) {
+        const uint32_t kb = sh.base + C::kOffK + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          ptx::mma_bf16(tmem + sb * kTileTok, ptx::sdesc_sw128(qbase + off, 16, 1024),
+                        ptx::sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        issued = true;
+      }
+      ptx::mma_commit(B.s_full(sb));
+      if (j > 0) issue_pv(j - 1);
+    }
+    issue_pv(T - 1);
+    ptx::mma_commit(B.o_full());
+    g += T;
+    gm += T;
+    ++nu;
+  }
+  if (*sh.abort_flag && issued) {
+    ptx::mma_commit(B.drain());
+    drain_wait(B.drain(), 0, kDrainLimitNs);
+  }
+}
+
+// ============================================================== compute warps
+// Shared-memory offset of element [row][col] (col in 0..63 of one 128-byte
+// swizzled half) for 8-element chunk granularity.
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <int D>
+__device__ void write_row_out(const AttnParams& p, const UnitDesc& u, int grow, const float* o,
+                              float inv, float lse2) {
+  const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
+  const int h = u.kvh * p.gqa + grow % p.gqa;
+  float* dst;
+  if (gt.pbase < 0) {
+    dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
+    if (p.lse) p.lse[(size_t)gt.tok * p.hq + h] = lse2 * kLn2;
+  } else {
+    const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
+    dst = p.part_o + slot * D;
+    p.part_lse[slot] = lse2;
+  }
+#pragma unroll
+  for (int c = 0; c < D; c += 4)
+    *reinterpret_cast<float4*>(dst + c) =
+        make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+}
+
+// CUDA-core consumer for a thin unit (<= 8 rows).
+template <int D>
+__device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, int T,
+                          const Shared& sh, const Bars<D>& B) {
+  using C = Cfg<D>;
+  constexpr int EPL = D / 32;
+  constexpr int RB = kSimtTileRows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nr = min(RB, u.nrows);
+  float qv[RB][EPL], o[RB][EPL], m[RB], l[RB];
+  int vis[RB];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+    vis[i] = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[i][e] = qv[i][e] = 0.f;
+    if (i < nr) {
+      const int grow = u.row0 + i;
+      const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
+      const int h = u.kvh * p.gqa + grow % p.gqa;
+      vis[i] = gt.vis;
+      const uint16_t* src = p.q + ((size_t)gt.tok * p.hq + h) * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+        qv[i][0] = bf16_lo(w.x) * p.scale_log2;
+        qv[i][1] = bf16_hi(w.x) * p.scale_log2;
+        qv[i][2] = bf16_lo(w.y) * p.scale_log2;
+        qv[i][3] = bf16_hi(w.y) * p.scale_log2;
+      } else {
+        const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(src));
+        qv[i][0] = bf16_lo(w) * p.scale_log2;
+        qv[i][1] = bf16_hi(w) * p.scale_log2;
+      }
+    }
+  }
+  // lane's slice inside a swizzled 128-byte row
+  const int half = (EPL == 4) ? (lane >> 4) : 0;
+  const int chunk = (EPL == 4) ? ((lane & 15) >> 1) : (lane >> 2);
+  const int inb = (EPL == 4) ? (lane & 1) * 8 : (lane & 3) * 4;
+  for (int j = 0; j < T; ++j) {
+    const int s = (g + j) % C::kStages;
+    const bool ok = wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+    const int b0 = u.blk0 + 8 * j;
+    const int nb = min(8, u.blk1 - b0);
+    const uint8_t* kst = sh.ptr + C::kOffK + s * C::kTileBytes + half * (kTileTok * 128) + inb;
+    const uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes + half * (kTileTok * 128) + inb;
+    if (ok) {
+      for (int bb = warp; bb < nb; bb += 4) {
+        const int2 bl = p.blocks[b0 + bb];
+        const int pos = bl.y >> 5, nvalid = bl.y & 31;
+        int tmax = 0;
+#pragma unroll
+        for (int i = 0; i < RB; ++i)
+          if (i < nr) tmax = max(tmax, min(nvalid, vis[i] - pos));
+        for (int t = 0; t < tmax; ++t) {
+          const int r = bb * 16 + t;
+          float kf[EPL], vf[EPL];
+          if constexpr (EPL == 4) {
+            const uint2 kw = *reinterpret_cast<const uint2*>(kst + sw128(r, chunk));
+            const uint2 vw = *reinterpret_cast<const uint2*>(vst + sw128(r, chunk));
+            kf[0] = bf16_lo(kw.x); kf[1] = bf16_hi(kw.x); kf[2] = bf16_lo(kw.y); kf[3] = bf16_hi(kw.y);
+            vf[0] = bf16_lo(vw.x); vf[1] = bf16_hi(vw.x); vf[2] = bf16_lo(vw.y); vf[3] = bf16_hi(vw.y);
+          } else {
+            const uint32_t kw = *reinterpret_cast<const uint32_t*>(kst + sw128(r, chunk));
+            const uint32_t vw = *reinterpret_cast<const uint32_t*>(vst + sw128(r, chunk));
+            kf[0] = bf16_lo(kw); kf[1] = bf16_hi(kw);
+            vf[0] = bf16_lo(vw); vf[1] = bf16_hi(vw);
+          }
+#pragma unroll
+          for (int i = 0; i < RB; ++i) {
+            if (i < nr && pos + t < vis[i]) {  // warp-uniform
+              float dot = 0.f;
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) dot = fmaf(qv[i][e], kf[e], dot);
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+              const float mn = fmaxf(m[i], dot);
+              const float alpha = ptx::ex2(m[i] - mn);
+              const float pr = ptx::ex2(dot - mn);
+              l[i] = fmaf(l[i], alpha, pr);
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) o[i][e] = fmaf(o[i][e], alpha, pr * vf[e]);
+              m[i] = mn;
+            }
+          }
+        }
+      }
+    }
+    ptx::named_bar_sync(1, kComputeThreads);
+    if (tid == 0) ptx::mbar_arrive(B.empty(s));
+  }
+  // combine the four warps' states (scratch in the P buffer, idle here)
+  float* sm_o = reinterpret_cast<float*>(sh.ptr + C::kOffP);  // [4][RB][D]
+  float* sm_ml = sm_o + 4 * RB * D;                            // [4][RB][2]
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    if (lane == 0) {
+      sm_ml[(warp * RB + i) * 2 + 0] = m[i];
+      sm_ml[(warp * RB + i) * 2 + 1] = l[i];
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) sm_o[(warp * RB + i) * D + lane * EPL + e] = o[i][e];
+  }
+  ptx::named_bar_sync(1, kComputeThreads);
+  for (int i = warp; i < nr; i += 4) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_ml[(w * RB + i) * 2]);
+    float L = 0.f, O[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) O[e] = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float sc = ptx::ex2(sm_ml[(w * RB + i) * 2] - M);
+        L = fmaf(sm_ml[(w * RB + i) * 2 + 1], sc, L);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) O[e] = fmaf(sm_o[(w * RB + i) * D + lane * EPL + e], sc, O[e]);
+      }
+    }
+    if (!*sh.abort_flag) {
+      const int grow = u.row0 + i;
+      const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
+      const int h = u.kvh * p.gqa + grow % p.gqa;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float lse2 = L > 0.f ? M + __log2f(L) : -INFINITY;
+      float* dst;
+      if (gt.pbase < 0) {
+        dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
+        if (lane == 0 && p.lse) p.lse[(size_t)gt.tok * p.hq + h] = lse2 * kLn2;
+      } else {
+        const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
+        dst = p.part_o + slot * D;
+        if (lane == 0) p.part_lse[slot] = lse2;
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = O[e] * inv;
+    }
+  }
+  ptx::named_bar_sync(1, kComputeThreads);
+}
+
+template <int D>
+__device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared& sh,
+                              const Bars<D>& B, uint32_t tmem) {
+  using C = Cfg<D>;
+  const int tid = threadIdx.x;  // query row within the tile / TMEM lane
+  const int warp = tid >> 5;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  uint32_t g = 0, gm = 0, nu = 0;
+  for (int ui = u0; ui < u1; ++ui) {
+    const UnitDesc u = p.units[p.cta_units[ui]];
+    const int T = unit_tiles(u);
+    if (T == 0) {  // empty span: every row sees nothing
+      if (tid < u.nrows && !*sh.abort_flag) {
+        float z[D];
+#pragma unroll
+        for (int c = 0; c < D; ++c) z[c] = 0.f;
+        write_row_out<D>(p, u, u.row0 + tid, z, 0.f, -INFINITY);
+      }
+      continue;
+    }
+    if (u.path != kPathMma) {
+      simt_unit<D>(p, u, g, T, sh, B);
+      g += T;
+      continue;
+    }
+    // ---- query tile: row tid (zeros past the unit's rows)
+    const bool row_ok = tid < u.nrows;
+    int vis = 0;
+    {
+      uint4 w[D / 8];
+      if (row_ok) {
+        const int grow = u.row0 + tid;
+        const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
+        const int h = u.kvh * p.gqa + grow % p.gqa;
+        vis = gt.vis;
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)gt.tok * p.hq + h) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) w[c] = __ldg(src + c);
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) w[c] = make_uint4(0, 0, 0, 0);
+      }
+      const uint32_t qb = sh.base + C::kOffQ;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        ptx::st_shared_v4(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), w[c].x, w[c].y, w[c].z,
+                          w[c].w);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(B.q_full());
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < T; ++j) {
+      const int s = (g + j) % C::kStages;
+      const int sb = (gm + j) & 1;
+      bool ok = wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+      ok = ok && wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      ptx::tc_fence_after();
+      const int b0 = u.blk0 + 8 * j;
+      const int nb = min(8, u.blk1 - b0);
+      int lim[8];
+      bool partial = false;
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) {
+        lim[bb] = 0;
+        if (bb < nb) {
+          const int2 bl = p.blocks[b0 + bb];
+          const int pos = bl.y >> 5, nvalid = bl.y & 31;
+          partial |= nvalid < 16;
+          if (row_ok) lim[bb] = max(0, min(nvalid, vis - pos));
+        }
+      }
+      float sv[kTileTok];
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < kTileTok / 32; ++c) {
+          float t32[32];
+          ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + c * 32, t32);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t32[e];
+        }
+        ptx::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(B.s_free(sb));
+      // masked row max (scores in log2 units)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTileTok; ++c)
+        if ((c & 15) < lim[c >> 4]) mx = fmaxf(mx, sv[c]);
+      mx *= p.scale_log2;
+      float m_new = m_run, alpha = 1.f;
+      if (mx > m_run + kRescaleLog2) {
+        m_new = mx;
+        alpha = ptx::ex2(m_run - m_new);
+      }
+      uint32_t pk[kTileTok / 2];
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kTileTok; c += 2) {
+        float a = ((c & 15) < lim[c >> 4]) ? ptx::ex2(fmaf(sv[c], p.scale_log2, -m_new)) : 0.f;
+        float b = (((c + 1) & 15) < lim[(c + 1) >> 4]) ? ptx::ex2(fmaf(sv[c + 1], p.scale_log2, -m_new)) : 0.f;
+        pk[c >> 1] = ptx::pack_bf16(a, b);
+        psum += bf16_lo(pk[c >> 1]) + bf16_hi(pk[c >> 1]);
+      }
+      l_run = fmaf(l_run, alpha, psum);
+      m_run = m_new;
+      // P buffer and O are free once the previous P.V has completed
+      ok = wait_bar(B.p_empty(), (gm + j + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
+      ok = __all_sync(0xffffffffu, ok);
+      ptx::tc_fence_after();
+      if (ok && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float t32[32];
+          const uint32_t ta = tmem + lane_base + 256 + c * 32;
+          ptx::tmem_ld32(ta, t32);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) t32[e] *= alpha;
+          ptx::tmem_st32(ta, t32);
+        }
+        ptx::tmem_wait_st();
+      }
+      {
+        const uint32_t pb = sh.base + C::kOffP;
+#pragma unroll
+        for (int c = 0; c < kTileTok / 8; ++c)
+          ptx::st_shared_v4(pb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), pk[4 * c], pk[4 * c + 1],
+                            pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      if (partial) {
+        // zero the V rows of page slots that hold no token (they may hold
+        // anything; P is 0 there but 0 * NaN is not 0)
+        uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes;
+        for (int idx = tid; idx < nb * 16 * C::kHalves * 8; idx += kComputeThreads) {
+          const int ch = idx & 7, r = (idx >> 3) % (nb * 16), hh = (idx >> 3) / (nb * 16);
+          const int nvalid = p.blocks[b0 + (r >> 4)].y & 31;
+          if ((r & 15) >= nvalid)
+            *reinterpret_cast<uint4*>(vst + hh * (kTileTok * 128) + r * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(B.p_full());
+    }
+    // ---- epilogue: O / l
+    bool ok = wait_bar(B.o_full(), nu & 1, sh, p.err, p.wait_timeout_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    ptx::tc_fence_after();
+    if (ok) {
+      float o[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float t32[32];
+        ptx::tmem_ld32(tmem + lane_base + 256 + c * 32, t32);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[c * 32 + e] = t32[e];
+      }
+      ptx::tmem_wait_ld();
+      if (row_ok && !*sh.abort_flag) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float lse2 = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
+        write_row_out<D>(p, u, u.row0 + tid, o, inv, lse2);
+      }
+    }
+    ptx::tc_fence_before();
+    g += T;
+    gm += T;
+    ++nu;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tree_attn_kernel(const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  Shared sh;
+  {
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t pad = (1024 - (raw & 1023)) & 1023;
+    sh.base = raw + pad;
+    sh.ptr = smem_raw + pad;
+  }
+  Bars<D> B{sh.base + C::kOffBar};
+  sh.tmem_slot = reinterpret_cast<volatile uint32_t*>(sh.ptr + C::kOffBar + C::kNumBars * 8);
+  sh.abort_flag = reinterpret_cast<volatile int*>(sh.ptr + C::kOffBar + C::kNumBars * 8 + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u0 = p.cta_off[blockIdx.x], u1 = p.cta_off[blockIdx.x + 1];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(B.full(s), 1);
+      ptx::mbar_init(B.empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(B.s_full(i), 1);
+      ptx::mbar_init(B.s_free(i), kComputeThreads);
+    }
+    ptx::mbar_init(B.p_full(), kComputeThreads);
+    ptx::mbar_init(B.p_empty(), 1);
+    ptx::mbar_init(B.q_full(), kComputeThreads);
+    ptx::mbar_init(B.o_full(), 1);
+    ptx::mbar_init(B.drain(), 1);
+    *sh.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    ptx::prefetch_tmap(&tmk);
+    ptx::prefetch_tmap(&tmv);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(sh.base + C::kOffBar + C::kNumBars * 8, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *sh.tmem_slot;
+
+  if (warp < 4) {
+    compute_warps<D>(p, u0, u1, sh, B, tmem);
+  } else if (warp == kProducerWarp) {
+    if (lane == 0) producer<D>(&tmk, &tmv, p, u0, u1, sh, B);
+    __syncwarp();
+  } else {
+    if (lane == 0) mma_issuer<D>(p, u0, u1, sh, B, tmem);
+    __syncwarp();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Page pool [pages][hkv][16][d] bf16 as a 4-D tensor (d, slot, head, page);
+// one box = one 64-column half of one page-head, 128-byte swizzle.
+cudaError_t make_page_map(CUtensorMap* m, const void* base, int d, int hkv, int num_pages) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[4] = {(cuuint64_t)d, 16, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)16 * d * 2, (cuuint64_t)hkv * 16 * d * 2};
+  cuuint32_t box[4] = {64, 16, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams& p, int grid, int num_pages, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap mk, mv;
+  memset(&mk, 0, sizeof mk);
+  memset(&mv, 0, sizeof mv);
+  if (num_pages > 0) {
+    cudaError_t e = make_page_map(&mk, p.k, D, p.hkv, num_pages);
+    if (e != cudaSuccess) return e;
+    e = make_page_map(&mv, p.v, D, p.hkv, num_pages);
+    if (e != cudaSuccess) return e;
+  }
+  tree_attn_kernel<D><<<grid, kThreads, Cfg<D>::kSmem, s>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tree_attention(const AttnParams& p, int d, int grid, int num_pages,
+                                  cudaStream_t s) {
+  if (p.n_units == 0 || grid == 0) return cudaSuccess;
+  return d == 128 ? launch_d<128>(p, grid, num_pages, s) : launch_d<64>(p, grid, num_pages, s);
+}
+
+}  // namespace ta
