@@ -302,7 +302,8 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
   const int inb = (EPL == 4) ? (lane & 1) * 8 : (lane & 3) * 4;
   for (int j = 0; j < T; ++j) {
     const int s = (g + j) % C::kStages;
-    const bool ok = wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+    const bool ok = __all_sync(
+        0xffffffffu, wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns));
     const int b0 = u.blk0 + 8 * j;
     const int nb = min(8, u.blk1 - b0);
     const uint8_t* kst = sh.ptr + C::kOffK + s * C::kTileBytes + half * (kTileTok * 128) + inb;
@@ -453,7 +454,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(B.q_full());
     }
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
       const int sb = (gm + j) & 1;
@@ -502,16 +503,20 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         m_new = mx;
         alpha = ptx::ex2(m_run - m_new);
       }
+      // P rounds to bf16 for the tensor cores; O is normalised by the sum of
+      // the rounded weights (the weights the MMA used), lse by the exact sum.
       uint32_t pk[kTileTok / 2];
-      float psum = 0.f;
+      float psum = 0.f, psum_exact = 0.f;
 #pragma unroll
       for (int c = 0; c < kTileTok; c += 2) {
         float a = ((c & 15) < lim[c >> 4]) ? ptx::ex2(fmaf(sv[c], p.scale_log2, -m_new)) : 0.f;
         float b = (((c + 1) & 15) < lim[(c + 1) >> 4]) ? ptx::ex2(fmaf(sv[c + 1], p.scale_log2, -m_new)) : 0.f;
         pk[c >> 1] = ptx::pack_bf16(a, b);
         psum += bf16_lo(pk[c >> 1]) + bf16_hi(pk[c >> 1]);
+        psum_exact += a + b;
       }
       l_run = fmaf(l_run, alpha, psum);
+      l_exact = fmaf(l_exact, alpha, psum_exact);
       m_run = m_new;
       // P buffer and O are free once the previous P.V has completed
       ok = wait_bar(B.p_empty(), (gm + j + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
@@ -569,7 +574,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       ptx::tmem_wait_ld();
       if (row_ok && !*sh.abort_flag) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const float lse2 = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
+        const float lse2 = l_exact > 0.f ? m_run + __log2f(l_exact) : -INFINITY;
         write_row_out<D>(p, u, u.row0 + tid, o, inv, lse2);
       }
     }
