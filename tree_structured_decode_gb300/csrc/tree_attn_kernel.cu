@@ -53,16 +53,17 @@ template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kStages = D == 128 ? 2 : 4;
-  static constexpr int kQBytes = 128 * D * 2;
+  static constexpr int kQBytes = 128 * D * 2;          // one query tile
   static constexpr int kTileBytes = kTileTok * D * 2;  // K (or V) of one tile
   static constexpr int kPBytes = 128 * kTileTok * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffQ = 0;                      // two query tiles
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffP = kOffV + kStages * kTileBytes;
   static constexpr int kOffBar = kOffP + kPBytes;
-  static constexpr int kNumBars = 2 * kStages + 9;
-  static constexpr int kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1024-B alignment slack
+  static constexpr int kNumBars = 2 * kStages + 10;
+  static constexpr int kOffMeta = kOffBar + kNumBars * 8 + 16;     // int [kStages][8]
+  static constexpr int kSmem = kOffMeta + kStages * 8 * 4 + 1024;   // + 1024-B alignment slack
   static constexpr uint32_t kBlockBytes = 16 * D * 2;                // one page-head
   static constexpr uint32_t kIdescQK = ptx::idesc_bf16(128, kTileTok, 0);
   static constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, D, 1);
@@ -71,6 +72,7 @@ struct Cfg {
 struct Shared {
   uint32_t base;  // 1024-aligned shared address of the layout
   uint8_t* ptr;
+  int* meta;      // [stage][8]: span position * 32 + valid slots of each block
   volatile uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
@@ -84,9 +86,9 @@ struct Bars {
   __device__ uint32_t s_free(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 2 + i); }
   __device__ uint32_t p_full() const { return b + 8 * (2 * Cfg<D>::kStages + 4); }
   __device__ uint32_t p_empty() const { return b + 8 * (2 * Cfg<D>::kStages + 5); }
-  __device__ uint32_t q_full() const { return b + 8 * (2 * Cfg<D>::kStages + 6); }
-  __device__ uint32_t o_full() const { return b + 8 * (2 * Cfg<D>::kStages + 7); }
-  __device__ uint32_t drain() const { return b + 8 * (2 * Cfg<D>::kStages + 8); }
+  __device__ uint32_t o_full() const { return b + 8 * (2 * Cfg<D>::kStages + 6); }
+  __device__ uint32_t drain() const { return b + 8 * (2 * Cfg<D>::kStages + 7); }
+  __device__ uint32_t q_full(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 8 + i); }
 };
 
 // Bounded wait.  Returns false (and does not wait) once the CTA has aborted;
@@ -136,21 +138,29 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     const UnitDesc u = p.units[p.cta_units[ui]];
     for (int b0 = u.blk0; b0 < u.blk1; b0 += 8, ++g) {
       const int s = g % C::kStages;
+      const int nb = min(8, u.blk1 - b0);
+      int2 bl[8];  // all eight loads in flight while waiting for the stage
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb)
+        bl[bb] = bb < nb ? __ldg(&p.blocks[b0 + bb]) : make_int2(0, 0);
       if (g >= (uint32_t)C::kStages &&
           !wait_bar(B.empty(s), ((g / C::kStages) + 1) & 1, sh, p.err, p.wait_timeout_ns))
         continue;
       if (*sh.abort_flag) continue;
-      const int nb = min(8, u.blk1 - b0);
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) sh.meta[s * 8 + bb] = bl[bb].y;
       ptx::mbar_arrive_expect_tx(B.full(s), (uint32_t)nb * 2u * C::kBlockBytes);
       const uint32_t kdst = sh.base + C::kOffK + s * C::kTileBytes;
       const uint32_t vdst = sh.base + C::kOffV + s * C::kTileBytes;
-      for (int bb = 0; bb < nb; ++bb) {
-        const int page = p.blocks[b0 + bb].x;
 #pragma unroll
-        for (int h = 0; h < C::kHalves; ++h) {
-          const uint32_t off = h * (kTileTok * 128) + bb * (16 * 128);
-          ptx::tma_load_4d(kdst + off, tmk, 64 * h, 0, u.kvh, page, B.full(s));
-          ptx::tma_load_4d(vdst + off, tmv, 64 * h, 0, u.kvh, page, B.full(s));
+      for (int bb = 0; bb < 8; ++bb) {
+        if (bb < nb) {
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) {
+            const uint32_t off = h * (kTileTok * 128) + bb * (16 * 128);
+            ptx::tma_load_4d(kdst + off, tmk, 64 * h, 0, u.kvh, bl[bb].x, B.full(s));
+            ptx::tma_load_4d(vdst + off, tmv, 64 * h, 0, u.kvh, bl[bb].x, B.full(s));
+          }
         }
       }
 #pragma unroll
@@ -182,8 +192,10 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       g += T;
       continue;
     }
-    const bool qok = wait_bar(B.q_full(), nu & 1, sh, p.err, p.wait_timeout_ns);
+    const bool qok = wait_bar(B.q_full(nu & 1), (nu >> 1) & 1, sh, p.err, p.wait_timeout_ns);
     ptx::tc_fence_after();
+    const uint32_t qb = qbase + (nu & 1) * C::kQBytes;
+    const uint32_t o_tmem = tmem + 256 + (nu & 1) * 128;
     auto issue_pv = [&](int jj) {
       const bool ok = wait_bar(B.p_full(), (gm + jj) & 1, sh, p.err, p.wait_timeout_ns);
       ptx::tc_fence_after();
@@ -194,7 +206,7 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
         for (int kk = 0; kk < nbk; ++kk) {
           const uint64_t ad = ptx::sdesc_sw128(pbase + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = ptx::sdesc_sw128(vb + kk * 2048, kTileTok * 128, 1024);
-          ptx::mma_bf16(tmem + 256, ad, bd, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16(o_tmem, ad, bd, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         issued = true;
       }
@@ -212,7 +224,7 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          ptx::mma_bf16(tmem + sb * kTileTok, ptx::sdesc_sw128(qbase + off, 16, 1024),
+          ptx::mma_bf16(tmem + sb * kTileTok, ptx::sdesc_sw128(qb + off, 16, 1024),
                         ptx::sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
         }
         issued = true;
@@ -257,6 +269,61 @@ __device__ void write_row_out(const AttnParams& p, const UnitDesc& u, int grow, 
   for (int c = 0; c < D; c += 4)
     *reinterpret_cast<float4*>(dst + c) =
         make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+}
+
+template <int EPL>
+__device__ __forceinline__ void load_slice(const uint8_t* ptr, float (&f)[EPL]) {
+  if constexpr (EPL == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(ptr);
+    f[0] = bf16_lo(w.x);
+    f[1] = bf16_hi(w.x);
+    f[2] = bf16_lo(w.y);
+    f[3] = bf16_hi(w.y);
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(ptr);
+    f[0] = bf16_lo(w);
+    f[1] = bf16_hi(w);
+  }
+}
+
+// Sum of v[t] over the 32 lanes for 16 values t at once (16 shuffles instead
+// of 16 x 5): after halving steps over lane bits 4..1 and a final exchange
+// over bit 0, lane L holds the total for t = L >> 1.
+__device__ __forceinline__ float transpose_sum16(float (&v)[16], int lane) {
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float send = up ? v[k] : v[k + 8];
+      const float keep = up ? v[k + 8] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float send = up ? v[k] : v[k + 4];
+      const float keep = up ? v[k + 4] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = up ? v[k] : v[k + 2];
+      const float keep = up ? v[k + 2] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+  }
+  {
+    const bool up = lane & 2;
+    const float send = up ? v[0] : v[1];
+    const float keep = up ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
 // CUDA-core consumer for a thin unit (<= 8 rows).
@@ -304,48 +371,50 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
     const int s = (g + j) % C::kStages;
     const bool ok = __all_sync(
         0xffffffffu, wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns));
-    const int b0 = u.blk0 + 8 * j;
-    const int nb = min(8, u.blk1 - b0);
+    const int nb = min(8, u.blk1 - (u.blk0 + 8 * j));
     const uint8_t* kst = sh.ptr + C::kOffK + s * C::kTileBytes + half * (kTileTok * 128) + inb;
     const uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes + half * (kTileTok * 128) + inb;
     if (ok) {
       for (int bb = warp; bb < nb; bb += 4) {
-        const int2 bl = p.blocks[b0 + bb];
-        const int pos = bl.y >> 5, nvalid = bl.y & 31;
-        int tmax = 0;
+        const int mt = sh.meta[s * 8 + bb];
+        const int pos = mt >> 5, nvalid = mt & 31;
 #pragma unroll
-        for (int i = 0; i < RB; ++i)
-          if (i < nr) tmax = max(tmax, min(nvalid, vis[i] - pos));
-        for (int t = 0; t < tmax; ++t) {
-          const int r = bb * 16 + t;
-          float kf[EPL], vf[EPL];
-          if constexpr (EPL == 4) {
-            const uint2 kw = *reinterpret_cast<const uint2*>(kst + sw128(r, chunk));
-            const uint2 vw = *reinterpret_cast<const uint2*>(vst + sw128(r, chunk));
-            kf[0] = bf16_lo(kw.x); kf[1] = bf16_hi(kw.x); kf[2] = bf16_lo(kw.y); kf[3] = bf16_hi(kw.y);
-            vf[0] = bf16_lo(vw.x); vf[1] = bf16_hi(vw.x); vf[2] = bf16_lo(vw.y); vf[3] = bf16_hi(vw.y);
-          } else {
-            const uint32_t kw = *reinterpret_cast<const uint32_t*>(kst + sw128(r, chunk));
-            const uint32_t vw = *reinterpret_cast<const uint32_t*>(vst + sw128(r, chunk));
-            kf[0] = bf16_lo(kw); kf[1] = bf16_hi(kw);
-            vf[0] = bf16_lo(vw); vf[1] = bf16_hi(vw);
+        for (int i = 0; i < RB; ++i) {
+          const int lim = i < nr ? max(0, min(nvalid, vis[i] - pos)) : 0;
+          if (lim == 0) continue;  // warp-uniform
+          // 16 independent partial dots, then one transposed reduction:
+          // lane L ends with the score of token L >> 1 of the block.
+          float d[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            float kf[EPL];
+            load_slice<EPL>(kst + sw128(bb * 16 + t, chunk), kf);
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc = fmaf(qv[i][e], kf[e], acc);
+            d[t] = acc;
           }
+          const float sc = transpose_sum16(d, lane);
+          const bool valid = (lane >> 1) < lim;
+          float bm = valid ? sc : -INFINITY;
 #pragma unroll
-          for (int i = 0; i < RB; ++i) {
-            if (i < nr && pos + t < vis[i]) {  // warp-uniform
-              float dot = 0.f;
+          for (int off = 16; off > 1; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+          const float m_new = fmaxf(m[i], bm);
+          const float alpha = ptx::ex2(m[i] - m_new);
+          const float pl = valid ? ptx::ex2(sc - m_new) : 0.f;
+          float ps = pl;
 #pragma unroll
-              for (int e = 0; e < EPL; ++e) dot = fmaf(qv[i][e], kf[e], dot);
+          for (int off = 16; off > 1; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+          l[i] = fmaf(l[i], alpha, ps);
+          m[i] = m_new;
 #pragma unroll
-              for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-              const float mn = fmaxf(m[i], dot);
-              const float alpha = ptx::ex2(m[i] - mn);
-              const float pr = ptx::ex2(dot - mn);
-              l[i] = fmaf(l[i], alpha, pr);
+          for (int e = 0; e < EPL; ++e) o[i][e] *= alpha;
+          for (int t = 0; t < lim; ++t) {
+            const float pt = __shfl_sync(0xffffffffu, pl, 2 * t);
+            float vf[EPL];
+            load_slice<EPL>(vst + sw128(bb * 16 + t, chunk), vf);
 #pragma unroll
-              for (int e = 0; e < EPL; ++e) o[i][e] = fmaf(o[i][e], alpha, pr * vf[e]);
-              m[i] = mn;
-            }
+            for (int e = 0; e < EPL; ++e) o[i][e] = fmaf(pt, vf[e], o[i][e]);
           }
         }
       }
@@ -404,6 +473,34 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
   ptx::named_bar_sync(1, kComputeThreads);
 }
 
+// Next unit (list index >= k) that runs on tensor cores and has KV; -1 if none.
+__device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1) {
+  for (; k < u1; ++k) {
+    const UnitDesc u = p.units[p.cta_units[k]];
+    if (u.path == kPathMma && u.blk1 > u.blk0) return k;
+  }
+  return -1;
+}
+
+// Start copying unit k's query tile (row tid; zeros past its rows) into the
+// swizzled buffer at qb.  Completion: cp_async_wait_all().
+template <int D>
+__device__ __forceinline__ void prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
+  const UnitDesc u = p.units[p.cta_units[k]];
+  const bool row_ok = tid < u.nrows;
+  const uint16_t* src = p.q;
+  if (row_ok) {
+    const int grow = u.row0 + tid;
+    const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
+    const int h = u.kvh * p.gqa + grow % p.gqa;
+    src = p.q + ((size_t)gt.tok * p.hq + h) * D;
+  }
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c)
+    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), src + c * 8, row_ok ? 16u : 0u);
+  ptx::cp_async_commit();
+}
+
 template <int D>
 __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared& sh,
                               const Bars<D>& B, uint32_t tmem) {
@@ -411,7 +508,18 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
   const int tid = threadIdx.x;  // query row within the tile / TMEM lane
   const int warp = tid >> 5;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t qbuf0 = sh.base + C::kOffQ;
   uint32_t g = 0, gm = 0, nu = 0;
+  // the first tensor-core unit's query tile, before anything else
+  {
+    const int first = next_mma_unit(p, u0, u1);
+    if (first >= 0) {
+      prefetch_q<D>(p, first, qbuf0, tid);
+      ptx::cp_async_wait_all();
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(B.q_full(0));
+    }
+  }
   for (int ui = u0; ui < u1; ++ui) {
     const UnitDesc u = p.units[p.cta_units[ui]];
     const int T = unit_tiles(u);
@@ -429,31 +537,16 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       g += T;
       continue;
     }
-    // ---- query tile: row tid (zeros past the unit's rows)
+    // The next tensor-core unit's query tile streams into the other buffer
+    // while this unit runs (its previous user finished before our epilogue).
+    const int nxt = next_mma_unit(p, ui + 1, u1);
+    if (nxt >= 0) prefetch_q<D>(p, nxt, qbuf0 + ((nu + 1) & 1) * C::kQBytes, tid);
+
     const bool row_ok = tid < u.nrows;
+    const bool wact = warp * 32 < u.nrows;  // warps of padding rows only keep the barriers in step
     int vis = 0;
-    {
-      uint4 w[D / 8];
-      if (row_ok) {
-        const int grow = u.row0 + tid;
-        const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
-        const int h = u.kvh * p.gqa + grow % p.gqa;
-        vis = gt.vis;
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)gt.tok * p.hq + h) * D);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) w[c] = __ldg(src + c);
-      } else {
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) w[c] = make_uint4(0, 0, 0, 0);
-      }
-      const uint32_t qb = sh.base + C::kOffQ;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c)
-        ptx::st_shared_v4(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), w[c].x, w[c].y, w[c].z,
-                          w[c].w);
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(B.q_full());
-    }
+    if (row_ok) vis = p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa].vis;
+    const uint32_t o_tmem = tmem + lane_base + 256 + (nu & 1) * 128;
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
@@ -462,22 +555,21 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       ok = ok && wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
-      const int b0 = u.blk0 + 8 * j;
-      const int nb = min(8, u.blk1 - b0);
+      const int nb = min(8, u.blk1 - (u.blk0 + 8 * j));
       int lim[8];
       bool partial = false;
 #pragma unroll
       for (int bb = 0; bb < 8; ++bb) {
         lim[bb] = 0;
         if (bb < nb) {
-          const int2 bl = p.blocks[b0 + bb];
-          const int pos = bl.y >> 5, nvalid = bl.y & 31;
+          const int mt = sh.meta[s * 8 + bb];
+          const int pos = mt >> 5, nvalid = mt & 31;
           partial |= nvalid < 16;
           if (row_ok) lim[bb] = max(0, min(nvalid, vis - pos));
         }
       }
       float sv[kTileTok];
-      if (ok) {
+      if (ok && wact) {
 #pragma unroll
         for (int c = 0; c < kTileTok / 32; ++c) {
           float t32[32];
@@ -492,50 +584,56 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(B.s_free(sb));
-      // masked row max (scores in log2 units)
-      float mx = -INFINITY;
+      // masked row max, eight independent chains (scores in log2 units)
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kTileTok; ++c)
-        if ((c & 15) < lim[c >> 4]) mx = fmaxf(mx, sv[c]);
-      mx *= p.scale_log2;
+        if ((c & 15) < lim[c >> 4]) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+      const float mx =
+          fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
       float m_new = m_run, alpha = 1.f;
-      if (mx > m_run + kRescaleLog2) {
+      if (wact && mx > m_run + kRescaleLog2) {
         m_new = mx;
         alpha = ptx::ex2(m_run - m_new);
       }
       // P rounds to bf16 for the tensor cores; O is normalised by the sum of
       // the rounded weights (the weights the MMA used), lse by the exact sum.
       uint32_t pk[kTileTok / 2];
-      float psum = 0.f, psum_exact = 0.f;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f}, pe4[4] = {0.f, 0.f, 0.f, 0.f};
+      if (wact) {
 #pragma unroll
-      for (int c = 0; c < kTileTok; c += 2) {
-        float a = ((c & 15) < lim[c >> 4]) ? ptx::ex2(fmaf(sv[c], p.scale_log2, -m_new)) : 0.f;
-        float b = (((c + 1) & 15) < lim[(c + 1) >> 4]) ? ptx::ex2(fmaf(sv[c + 1], p.scale_log2, -m_new)) : 0.f;
-        pk[c >> 1] = ptx::pack_bf16(a, b);
-        psum += bf16_lo(pk[c >> 1]) + bf16_hi(pk[c >> 1]);
-        psum_exact += a + b;
+        for (int c = 0; c < kTileTok; c += 2) {
+          const float a = ((c & 15) < lim[c >> 4]) ? ptx::ex2(fmaf(sv[c], p.scale_log2, -m_new)) : 0.f;
+          const float b = (((c + 1) & 15) < lim[(c + 1) >> 4])
+                              ? ptx::ex2(fmaf(sv[c + 1], p.scale_log2, -m_new)) : 0.f;
+          pk[c >> 1] = ptx::pack_bf16(a, b);
+          ps4[(c >> 1) & 3] += bf16_lo(pk[c >> 1]) + bf16_hi(pk[c >> 1]);
+          pe4[(c >> 1) & 3] += a + b;
+        }
       }
-      l_run = fmaf(l_run, alpha, psum);
-      l_exact = fmaf(l_exact, alpha, psum_exact);
+      l_run = fmaf(l_run, alpha, (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+      l_exact = fmaf(l_exact, alpha, (pe4[0] + pe4[1]) + (pe4[2] + pe4[3]));
       m_run = m_new;
       // P buffer and O are free once the previous P.V has completed
       ok = wait_bar(B.p_empty(), (gm + j + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
-      if (ok && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float t32[32];
-          const uint32_t ta = tmem + lane_base + 256 + c * 32;
-          ptx::tmem_ld32(ta, t32);
+          ptx::tmem_ld32(o_tmem + c * 32, t32);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) t32[e] *= alpha;
-          ptx::tmem_st32(ta, t32);
+          ptx::tmem_st32(o_tmem + c * 32, t32);
         }
         ptx::tmem_wait_st();
       }
-      {
+      if (wact) {
         const uint32_t pb = sh.base + C::kOffP;
 #pragma unroll
         for (int c = 0; c < kTileTok / 8; ++c)
@@ -548,7 +646,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes;
         for (int idx = tid; idx < nb * 16 * C::kHalves * 8; idx += kComputeThreads) {
           const int ch = idx & 7, r = (idx >> 3) % (nb * 16), hh = (idx >> 3) / (nb * 16);
-          const int nvalid = p.blocks[b0 + (r >> 4)].y & 31;
+          const int nvalid = sh.meta[s * 8 + (r >> 4)] & 31;
           if ((r & 15) >= nvalid)
             *reinterpret_cast<uint4*>(vst + hh * (kTileTok * 128) + r * 128 + ch * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -558,16 +656,23 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       ptx::tc_fence_before();
       ptx::mbar_arrive(B.p_full());
     }
+    // the next unit's query tile is complete: hand it to the MMA issuer now,
+    // so its first QK^T overlaps this unit's epilogue
+    if (nxt >= 0) {
+      ptx::cp_async_wait_all();
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(B.q_full((nu + 1) & 1));
+    }
     // ---- epilogue: O / l
     bool ok = wait_bar(B.o_full(), nu & 1, sh, p.err, p.wait_timeout_ns);
     ok = __all_sync(0xffffffffu, ok);
     ptx::tc_fence_after();
-    if (ok) {
+    if (ok && wact) {
       float o[D];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float t32[32];
-        ptx::tmem_ld32(tmem + lane_base + 256 + c * 32, t32);
+        ptx::tmem_ld32(o_tmem + c * 32, t32);
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[c * 32 + e] = t32[e];
       }
@@ -601,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars<D> B{sh.base + C::kOffBar};
   sh.tmem_slot = reinterpret_cast<volatile uint32_t*>(sh.ptr + C::kOffBar + C::kNumBars * 8);
   sh.abort_flag = reinterpret_cast<volatile int*>(sh.ptr + C::kOffBar + C::kNumBars * 8 + 4);
+  sh.meta = reinterpret_cast<int*>(sh.ptr + C::kOffMeta);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u0 = p.cta_off[blockIdx.x], u1 = p.cta_off[blockIdx.x + 1];
 
@@ -615,7 +721,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(B.p_full(), kComputeThreads);
     ptx::mbar_init(B.p_empty(), 1);
-    ptx::mbar_init(B.q_full(), kComputeThreads);
+    ptx::mbar_init(B.q_full(0), kComputeThreads);
+    ptx::mbar_init(B.q_full(1), kComputeThreads);
     ptx::mbar_init(B.o_full(), 1);
     ptx::mbar_init(B.drain(), 1);
     *sh.abort_flag = 0;
