@@ -24,8 +24,7 @@ struct AttnParams {
   const UnitDesc* units;
   const int2* blocks;        // {page, span_pos * 32 + valid}
   const GroupTok* gtoks;
-  const int32_t* cta_off;    // persistent schedule
-  const int32_t* cta_units;
+  const int32_t* cta_off;    // CTA c runs units [cta_off[c], cta_off[c+1])
   const uint16_t* q;         // bf16 bits [nq][hq][d]
   const uint16_t* k;         // bf16 bits [pages][hkv][16][d]
   const uint16_t* v;

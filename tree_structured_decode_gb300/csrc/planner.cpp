@@ -379,11 +379,15 @@ tree_attn_status build_host_plan(
       lists[it.second].push_back(i);
       heap.push({it.first + cost(i), it.second});
     }
+    // store the units CTA-major: CTA c runs units [cta_off[c], cta_off[c+1])
     p.cta_off.assign(p.grid + 1, 0);
+    std::vector<UnitDesc> sched;
+    sched.reserve(nu);
     for (int32_t c = 0; c < p.grid; ++c) {
       p.cta_off[c + 1] = p.cta_off[c] + (int32_t)lists[c].size();
-      p.cta_units.insert(p.cta_units.end(), lists[c].begin(), lists[c].end());
+      for (int32_t i : lists[c]) sched.push_back(p.units[i]);
     }
+    p.units.swap(sched);
   }
   return TA_OK;
 }

@@ -83,8 +83,8 @@ struct HostPlan {
   std::vector<int32_t> pcount, poff;          // per query token
   int64_t n_partials = 0;
   std::vector<int32_t> merge_tok;             // tokens with >= 2 partials
-  std::vector<UnitDesc> units;
-  std::vector<int32_t> cta_off, cta_units;    // persistent schedule
+  std::vector<UnitDesc> units;                // in schedule order (CTA-major)
+  std::vector<int32_t> cta_off;               // CTA c runs units [cta_off[c], cta_off[c+1])
   int32_t grid = 0;
   // sizes
   int64_t unique_kv_tokens = 0, group_kv_tokens = 0, visible_pairs = 0;

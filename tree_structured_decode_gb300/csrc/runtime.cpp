@@ -24,7 +24,6 @@ struct tree_attn_plan_s {
   const int2* d_blocks = nullptr;
   const ta::GroupTok* d_gtoks = nullptr;
   const int32_t* d_cta_off = nullptr;
-  const int32_t* d_cta_units = nullptr;
   const ta::MergeItem* d_merge = nullptr;
   int32_t* d_err = nullptr;
   float* d_part_o = nullptr;
@@ -89,12 +88,11 @@ tree_attn_status upload(tree_attn_plan_s* P) {
     size_t bytes;
     size_t off;
   };
-  Sec secs[7] = {
+  Sec secs[6] = {
       {h.units.data(), h.units.size() * sizeof(ta::UnitDesc), 0},
       {blocks.data(), blocks.size() * sizeof(int2), 0},
       {gt.data(), gt.size() * sizeof(ta::GroupTok), 0},
       {h.cta_off.data(), h.cta_off.size() * sizeof(int32_t), 0},
-      {h.cta_units.data(), h.cta_units.size() * sizeof(int32_t), 0},
       {merge.data(), merge.size() * sizeof(ta::MergeItem), 0},
       {nullptr, 16 * sizeof(int32_t), 0},  // error word(s)
   };
@@ -119,9 +117,8 @@ tree_attn_status upload(tree_attn_plan_s* P) {
   P->d_blocks = reinterpret_cast<const int2*>(b + secs[1].off);
   P->d_gtoks = reinterpret_cast<const ta::GroupTok*>(b + secs[2].off);
   P->d_cta_off = reinterpret_cast<const int32_t*>(b + secs[3].off);
-  P->d_cta_units = reinterpret_cast<const int32_t*>(b + secs[4].off);
-  P->d_merge = reinterpret_cast<const ta::MergeItem*>(b + secs[5].off);
-  P->d_err = reinterpret_cast<int32_t*>(b + secs[6].off);
+  P->d_merge = reinterpret_cast<const ta::MergeItem*>(b + secs[4].off);
+  P->d_err = reinterpret_cast<int32_t*>(b + secs[5].off);
 
   const size_t np = (size_t)h.n_partials * h.hq;
   const size_t o_bytes = align_up(np * h.d * sizeof(float), 256);
@@ -251,7 +248,6 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
   ap.blocks = P->d_blocks;
   ap.gtoks = P->d_gtoks;
   ap.cta_off = P->d_cta_off;
-  ap.cta_units = P->d_cta_units;
   ap.q = static_cast<const uint16_t*>(q);
   ap.k = static_cast<const uint16_t*>(k_pages);
   ap.v = static_cast<const uint16_t*>(v_pages);

@@ -134,8 +134,10 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
   uint32_t filled[C::kStages];  // 1 + tile index of the last fill issued per stage
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) filled[s] = 0;
+  UnitDesc un = u0 < u1 ? p.units[u0] : UnitDesc{};
   for (int ui = u0; ui < u1; ++ui) {
-    const UnitDesc u = p.units[p.cta_units[ui]];
+    const UnitDesc u = un;
+    if (ui + 1 < u1) un = p.units[ui + 1];  // in flight while this unit is issued
     for (int b0 = u.blk0; b0 < u.blk1; b0 += 8, ++g) {
       const int s = g % C::kStages;
       const int nb = min(8, u.blk1 - b0);
@@ -185,8 +187,10 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
   const uint32_t qbase = sh.base + C::kOffQ;
   const uint32_t pbase = sh.base + C::kOffP;
   bool issued = false;
+  UnitDesc un = u0 < u1 ? p.units[u0] : UnitDesc{};
   for (int ui = u0; ui < u1; ++ui) {
-    const UnitDesc u = p.units[p.cta_units[ui]];
+    const UnitDesc u = un;
+    if (ui + 1 < u1) un = p.units[ui + 1];
     const int T = unit_tiles(u);
     if (u.path != kPathMma || T == 0) {
       g += T;
@@ -476,7 +480,7 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
 // Next unit (list index >= k) that runs on tensor cores and has KV; -1 if none.
 __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1) {
   for (; k < u1; ++k) {
-    const UnitDesc u = p.units[p.cta_units[k]];
+    const UnitDesc u = p.units[k];
     if (u.path == kPathMma && u.blk1 > u.blk0) return k;
   }
   return -1;
@@ -484,21 +488,25 @@ __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1)
 
 // Start copying unit k's query tile (row tid; zeros past its rows) into the
 // swizzled buffer at qb.  Completion: cp_async_wait_all().
+// Returns the row's visible end in the group span (0 past the unit's rows).
 template <int D>
-__device__ __forceinline__ void prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
-  const UnitDesc u = p.units[p.cta_units[k]];
+__device__ __forceinline__ int prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
+  const UnitDesc u = p.units[k];
   const bool row_ok = tid < u.nrows;
   const uint16_t* src = p.q;
+  int vis = 0;
   if (row_ok) {
     const int grow = u.row0 + tid;
     const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
     const int h = u.kvh * p.gqa + grow % p.gqa;
     src = p.q + ((size_t)gt.tok * p.hq + h) * D;
+    vis = gt.vis;
   }
 #pragma unroll
   for (int c = 0; c < D / 8; ++c)
     ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), src + c * 8, row_ok ? 16u : 0u);
   ptx::cp_async_commit();
+  return vis;
 }
 
 template <int D>
@@ -510,18 +518,21 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   const uint32_t qbuf0 = sh.base + C::kOffQ;
   uint32_t g = 0, gm = 0, nu = 0;
+  int vis_next = 0;  // visible end of this thread's row in the next tensor-core unit
   // the first tensor-core unit's query tile, before anything else
   {
     const int first = next_mma_unit(p, u0, u1);
     if (first >= 0) {
-      prefetch_q<D>(p, first, qbuf0, tid);
+      vis_next = prefetch_q<D>(p, first, qbuf0, tid);
       ptx::cp_async_wait_all();
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(B.q_full(0));
     }
   }
+  UnitDesc un = u0 < u1 ? p.units[u0] : UnitDesc{};
   for (int ui = u0; ui < u1; ++ui) {
-    const UnitDesc u = p.units[p.cta_units[ui]];
+    const UnitDesc u = un;
+    if (ui + 1 < u1) un = p.units[ui + 1];
     const int T = unit_tiles(u);
     if (T == 0) {  // empty span: every row sees nothing
       if (tid < u.nrows && !*sh.abort_flag) {
@@ -539,13 +550,12 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     }
     // The next tensor-core unit's query tile streams into the other buffer
     // while this unit runs (its previous user finished before our epilogue).
+    const int vis = vis_next;
     const int nxt = next_mma_unit(p, ui + 1, u1);
-    if (nxt >= 0) prefetch_q<D>(p, nxt, qbuf0 + ((nu + 1) & 1) * C::kQBytes, tid);
+    if (nxt >= 0) vis_next = prefetch_q<D>(p, nxt, qbuf0 + ((nu + 1) & 1) * C::kQBytes, tid);
 
     const bool row_ok = tid < u.nrows;
     const bool wact = warp * 32 < u.nrows;  // warps of padding rows only keep the barriers in step
-    int vis = 0;
-    if (row_ok) vis = p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa].vis;
     const uint32_t o_tmem = tmem + lane_base + 256 + (nu & 1) * 128;
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     for (int j = 0; j < T; ++j) {
@@ -731,6 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp && lane == 0) {
     ptx::prefetch_tmap(&tmk);
     ptx::prefetch_tmap(&tmv);
+  }
+  // Warm L2 with this CTA's tables (unit records, their block lists and row
+  // records): the roles then find them in L2 instead of DRAM.
+  for (int k = u0 + (int)threadIdx.x; k < u1; k += kThreads) {
+    const UnitDesc u = p.units[k];
+    for (int b = u.blk0; b < u.blk1; b += 16) ptx::prefetch_l2(&p.blocks[b]);
+    const int t0 = u.tok_off + u.row0 / p.gqa, t1 = u.tok_off + (u.row0 + u.nrows - 1) / p.gqa;
+    for (int t = t0; t <= t1; t += 8) ptx::prefetch_l2(&p.gtoks[t]);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(sh.base + C::kOffBar + C::kNumBars * 8, kTmemCols);
