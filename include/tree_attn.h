@@ -160,6 +160,37 @@ tree_attn_status tree_attn_run(tree_attn_plan_t plan, const void* q,
                                const void* k_pages, const void* v_pages,
                                float* out, float* lse, void* stream);
 
+/* Size of the scratch array compiled into the library for
+ * tree_attn_run_static(): 32 MiB, held on every GPU where that entry point's
+ * code is loaded, until the process exits. */
+#define TREE_ATTN_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* Run without allocating device memory.  The method's pages have no
+ * counterpart for this: it serves callers that may not call cudaMalloc, such
+ * as a plug-in whose host engine owns all device memory, or a serving loop
+ * whose memory budget was fixed at start-up.  Same arguments, results and
+ * asynchrony as tree_attn_run(), and `plan` may be a host_only plan (which
+ * holds no device memory), so planning and running allocate nothing on the
+ * GPU.  The plan's tables and its partial results go into one static
+ * scratch array of TREE_ATTN_STATIC_SCRATCH_BYTES; each call re-copies the
+ * tables (stream-ordered) and clears what must start at zero.
+ *   - The first call on a device looks up the scratch address on that
+ *     device (the device must be current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race and corrupt each other's results.
+ *     Serialise them, e.g. on one stream.
+ *   - A plan whose tables and partials exceed the scratch is rejected with
+ *     TA_ERR_UNSUPPORTED (tree_attn_last_error() gives the size it needs);
+ *     nothing is launched.
+ *   - In-kernel wait errors of this path are not reported through
+ *     tree_attn_device_status().
+ * Errors: as tree_attn_run(), plus TA_ERR_UNSUPPORTED (too large) and
+ * TA_ERR_CUDA (scratch lookup or copy failed). */
+tree_attn_status tree_attn_run_static(tree_attn_plan_t plan, const void* q,
+                                      const void* k_pages, const void* v_pages,
+                                      float* out, float* lse, void* stream);
+
 /* Wait for `stream`, then read and clear the plan's device error word.
  * *code receives a TA_DEVERR_* value; returns TA_ERR_DEVICE if it is not
  * TA_DEVERR_NONE, TA_ERR_CUDA if the stream reported an error. */

@@ -126,6 +126,17 @@ class Plan:
         check(st, "tree_attn_run")
         return out, lse
 
+    def run_static(self, q, k_pages, v_pages, out, lse, stream=None) -> int:
+        """tree_attn_run_static(): run without any device allocation (the
+        library's fixed scratch holds the tables and partial results).  For
+        callers that may not allocate device memory; ``out`` and ``lse`` must
+        be given.  Returns the status (0 = TA_OK); see include/tree_attn.h for
+        the size limit and the rule that calls must not overlap."""
+        return self._lib.tree_attn_run_static(
+            self._handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pages.data_ptr()),
+            ctypes.c_void_p(v_pages.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(lse.data_ptr() if lse is not None else 0), _stream_handle(stream))
+
     def run_ptrs(self, q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, lse_ptr: int,
                  stream_handle: int) -> int:
         """Raw-pointer run (no checks beyond the library's); returns the status."""

@@ -10,30 +10,8 @@
 
 #include "../../include/tree_attn.h"
 #include "kernels.h"
+#include "plan_state.h"
 #include "planner.h"
-
-struct tree_attn_plan_s {
-  ta::HostPlan hp;
-  bool host_only = true;
-  int device = -1;
-  void* dmeta = nullptr;
-  size_t meta_bytes = 0;
-  void* dwork = nullptr;
-  size_t work_bytes = 0;
-  const ta::UnitDesc* d_units = nullptr;
-  const int2* d_blocks = nullptr;
-  const ta::GroupTok* d_gtoks = nullptr;
-  const int32_t* d_cta_off = nullptr;
-  const ta::MergeItem* d_merge = nullptr;
-  int32_t* d_err = nullptr;
-  float* d_part_o = nullptr;
-  float* d_part_lse = nullptr;
-  double plan_ms = 0.0;
-  bool profiling = false;
-  bool profiled_run = false;
-  bool profiled_merge = false;
-  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
-};
 
 namespace {
 
@@ -152,6 +130,10 @@ void release(tree_attn_plan_s* P) {
 }
 
 }  // namespace
+
+namespace ta {
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace ta
 
 extern "C" {
 
