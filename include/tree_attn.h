@@ -92,6 +92,10 @@ typedef struct {
                                TA_DEVERR_TIMEOUT and return                   */
   const int8_t* force_edges;/* [NULL = greedy] per node 0/1 (root ignored):
                                use this edge assignment instead             */
+  int32_t debug_stuck_wait; /* [0] testing aid: 1 makes every CTA first wait
+                               on a barrier that nothing signals, so the
+                               kernel must take its timeout path (records
+                               TA_DEVERR_TIMEOUT, results undefined)        */
 } tree_attn_options;
 
 /* Sizes of a plan, for logging and roofline accounting. */

@@ -42,7 +42,7 @@ class PlannerOptions:
     mma_min_rows: int = 4                # rows per kv head to use tensor cores
     mma_tile_rows: int = 128             # MMA query tile (M)
     simt_tile_rows: int = 8              # CUDA-core query tile
-    kv_tile_tokens: int = 128            # chunk granularity (tokens)
+    kv_tile_tokens: int = 64             # chunk granularity (tokens)
     split_tokens: int = 0                # 0 = automatic split, < 0 = never
     min_split_tokens: int = 256          # smallest automatic chunk
     split_waves: int = 2                 # automatic split aims at waves x SMs

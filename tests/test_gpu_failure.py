@@ -1,7 +1,8 @@
 """Failure detection on the GPU without a fault: every in-kernel wait has a
-time limit; a limit so short that the first wait for a TMA copy runs out makes
-the kernel record TA_DEVERR_TIMEOUT, drain its copies in flight, free TMEM and
-return.  The host reads the status and the context stays usable."""
+time limit.  With debug_stuck_wait each CTA first waits on a barrier that
+nothing signals; the wait runs out (1 ms limit), the kernel records
+TA_DEVERR_TIMEOUT, stops issuing work, drains what is in flight, frees TMEM and
+returns.  The host reads the status and the context stays usable."""
 import pytest
 import torch
 
@@ -17,7 +18,7 @@ def test_expired_wait_is_reported_and_context_survives():
 
     spec = W.two_level(2048, 8, 100, 16, 4, 128, seed=9)
     q, k, v = make_inputs(spec)
-    with ta.Plan.from_spec(spec, wait_timeout_us=1) as p:
+    with ta.Plan.from_spec(spec, wait_timeout_us=1000, debug_stuck_wait=1) as p:
         p.run(q, k, v)
         code = p.device_status()
     assert code == _abi.DEVERR_TIMEOUT

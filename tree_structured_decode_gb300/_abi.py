@@ -46,6 +46,7 @@ class Options(ctypes.Structure):
         ("host_only", ctypes.c_int32),
         ("wait_timeout_us", ctypes.c_int32),
         ("force_edges", ctypes.POINTER(ctypes.c_int8)),
+        ("debug_stuck_wait", ctypes.c_int32),
     ]
 
 

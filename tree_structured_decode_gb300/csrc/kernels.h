@@ -36,6 +36,7 @@ struct AttnParams {
   int32_t hq, hkv, gqa, n_units;
   float scale_log2;          // softmax scale * log2(e)
   long long wait_timeout_ns;
+  int32_t debug_stuck_wait;  // testing aid: wait on a barrier nothing signals
 };
 
 struct MergeParams {

@@ -366,7 +366,10 @@ tree_attn_status build_host_plan(
   {
     std::vector<int32_t> order(nu);
     for (int64_t i = 0; i < nu; ++i) order[i] = (int32_t)i;
-    auto cost = [&](int32_t i) { return (int64_t)(p.units[i].blk1 - p.units[i].blk0) + 2; };
+    // blocks streamed plus a fixed start-up and epilogue cost per unit
+    auto cost = [&](int32_t i) {
+      return (int64_t)(p.units[i].blk1 - p.units[i].blk0) + (p.units[i].path == kPathMma ? 6 : 3);
+    };
     std::stable_sort(order.begin(), order.end(),
                      [&](int32_t a, int32_t b) { return cost(a) > cost(b); });
     using Item = std::pair<int64_t, int32_t>;  // (load, cta), min-heap

@@ -18,7 +18,7 @@
 namespace ta {
 
 constexpr int kPageSize = 16;
-constexpr int kKvTileTokens = 128;                 // one KV tile = 8 pages
+constexpr int kKvTileTokens = 64;                  // one KV tile = 4 pages
 constexpr int kBlocksPerTile = kKvTileTokens / kPageSize;
 constexpr int kMmaTileRows = 128;                  // tcgen05 M
 constexpr int kSimtTileRows = 8;                   // CUDA-core rows per unit
@@ -39,6 +39,7 @@ struct Options {
   int32_t host_only = 0;
   int32_t wait_timeout_us = 2000000;
   std::vector<int8_t> force_edges;  // empty = greedy
+  int32_t debug_stuck_wait = 0;
 };
 
 // One work unit as the kernels read it (32 bytes, device POD).

@@ -44,6 +44,7 @@ ta::Options to_options(const tree_attn_options* o) {
   r.force_path = o->force_path;
   r.host_only = o->host_only;
   if (o->wait_timeout_us) r.wait_timeout_us = o->wait_timeout_us;
+  r.debug_stuck_wait = o->debug_stuck_wait;
   return r;
 }
 
@@ -244,6 +245,7 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
   ap.n_units = (int32_t)h.units.size();
   ap.scale_log2 = h.scale * 1.4426950408889634f;
   ap.wait_timeout_ns = (long long)h.opt.wait_timeout_us * 1000ll;
+  ap.debug_stuck_wait = h.opt.debug_stuck_wait;
   cudaError_t e;
   if (P->profiling) {
     e = cudaEventRecord(P->ev[0], s);

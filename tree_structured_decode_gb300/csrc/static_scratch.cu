@@ -185,6 +185,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   ap.n_units = (int32_t)nu;
   ap.scale_log2 = h.scale * 1.4426950408889634f;
   ap.wait_timeout_ns = (long long)h.opt.wait_timeout_us * 1000ll;
+  ap.debug_stuck_wait = h.opt.debug_stuck_wait;
   e = launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
   if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("partial attention launch: ") + cudaGetErrorString(e));
   if (nmerge) {

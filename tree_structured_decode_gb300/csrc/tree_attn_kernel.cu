@@ -43,7 +43,8 @@ constexpr int kThreads = 192;
 constexpr int kComputeThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kTileTok = 128;
+constexpr int kTileTok = kKvTileTokens;  // KV tokens per tile (4 pages)
+constexpr int kBpt = kTileTok / 16;       // pages (blocks) per tile
 constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint32_t kTmemCols = 512;
@@ -52,7 +53,7 @@ constexpr long long kDrainLimitNs = 200000000;  // 200 ms for copies / MMAs alre
 template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kQBytes = 128 * D * 2;          // one query tile
   static constexpr int kTileBytes = kTileTok * D * 2;  // K (or V) of one tile
   static constexpr int kPBytes = 128 * kTileTok * 2;
@@ -61,9 +62,12 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffP = kOffV + kStages * kTileBytes;
   static constexpr int kOffBar = kOffP + kPBytes;
-  static constexpr int kNumBars = 2 * kStages + 10;
-  static constexpr int kOffMeta = kOffBar + kNumBars * 8 + 16;     // int [kStages][8]
-  static constexpr int kSmem = kOffMeta + kStages * 8 * 4 + 1024;   // + 1024-B alignment slack
+  static constexpr int kNumBars = 2 * kStages + 11;
+  static constexpr int kOffMeta = kOffBar + kNumBars * 8 + 16;     // int [kStages][kBpt]
+  static constexpr int kOffML = kOffMeta + kStages * kBpt * 4;      // float [4][8][2]
+  static constexpr int kSmem = kOffML + 4 * kSimtTileRows * 2 * 4 + 1024;  // + alignment slack
+  // the CUDA-core path combines its four warps' O in the (idle) P buffer
+  static_assert(4 * kSimtTileRows * D * 4 <= kPBytes, "combine scratch exceeds the P buffer");
   static constexpr uint32_t kBlockBytes = 16 * D * 2;                // one page-head
   static constexpr uint32_t kIdescQK = ptx::idesc_bf16(128, kTileTok, 0);
   static constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, D, 1);
@@ -72,7 +76,7 @@ struct Cfg {
 struct Shared {
   uint32_t base;  // 1024-aligned shared address of the layout
   uint8_t* ptr;
-  int* meta;      // [stage][8]: span position * 32 + valid slots of each block
+  int* meta;      // [stage][kBpt]: span position * 32 + valid slots of each block
   volatile uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
@@ -89,6 +93,7 @@ struct Bars {
   __device__ uint32_t o_full() const { return b + 8 * (2 * Cfg<D>::kStages + 6); }
   __device__ uint32_t drain() const { return b + 8 * (2 * Cfg<D>::kStages + 7); }
   __device__ uint32_t q_full(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 8 + i); }
+  __device__ uint32_t never() const { return b + 8 * (2 * Cfg<D>::kStages + 10); }
 };
 
 // Bounded wait.  Returns false (and does not wait) once the CTA has aborted;
@@ -119,7 +124,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
 }
 
 __device__ __forceinline__ int unit_tiles(const UnitDesc& u) {
-  return (u.blk1 - u.blk0 + 7) >> 3;
+  return (u.blk1 - u.blk0 + kBpt - 1) / kBpt;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -131,6 +136,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                          int u0, int u1, const Shared& sh, const Bars<D>& B) {
   using C = Cfg<D>;
   uint32_t g = 0;
+  if (p.debug_stuck_wait) wait_bar(B.never(), 0, sh, p.err, p.wait_timeout_ns);
   uint32_t filled[C::kStages];  // 1 + tile index of the last fill issued per stage
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) filled[s] = 0;
@@ -138,24 +144,24 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
   for (int ui = u0; ui < u1; ++ui) {
     const UnitDesc u = un;
     if (ui + 1 < u1) un = p.units[ui + 1];  // in flight while this unit is issued
-    for (int b0 = u.blk0; b0 < u.blk1; b0 += 8, ++g) {
+    for (int b0 = u.blk0; b0 < u.blk1; b0 += kBpt, ++g) {
       const int s = g % C::kStages;
-      const int nb = min(8, u.blk1 - b0);
-      int2 bl[8];  // all eight loads in flight while waiting for the stage
+      const int nb = min(kBpt, u.blk1 - b0);
+      int2 bl[kBpt];  // all loads in flight while waiting for the stage
 #pragma unroll
-      for (int bb = 0; bb < 8; ++bb)
+      for (int bb = 0; bb < kBpt; ++bb)
         bl[bb] = bb < nb ? __ldg(&p.blocks[b0 + bb]) : make_int2(0, 0);
       if (g >= (uint32_t)C::kStages &&
           !wait_bar(B.empty(s), ((g / C::kStages) + 1) & 1, sh, p.err, p.wait_timeout_ns))
         continue;
       if (*sh.abort_flag) continue;
 #pragma unroll
-      for (int bb = 0; bb < 8; ++bb) sh.meta[s * 8 + bb] = bl[bb].y;
+      for (int bb = 0; bb < kBpt; ++bb) sh.meta[s * kBpt + bb] = bl[bb].y;
       ptx::mbar_arrive_expect_tx(B.full(s), (uint32_t)nb * 2u * C::kBlockBytes);
       const uint32_t kdst = sh.base + C::kOffK + s * C::kTileBytes;
       const uint32_t vdst = sh.base + C::kOffV + s * C::kTileBytes;
 #pragma unroll
-      for (int bb = 0; bb < 8; ++bb) {
+      for (int bb = 0; bb < kBpt; ++bb) {
         if (bb < nb) {
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h) {
@@ -204,7 +210,7 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       const bool ok = wait_bar(B.p_full(), (gm + jj) & 1, sh, p.err, p.wait_timeout_ns);
       ptx::tc_fence_after();
       const int s = (g + jj) % C::kStages;
-      const int nbk = min(8, u.blk1 - (u.blk0 + 8 * jj));
+      const int nbk = min(kBpt, u.blk1 - (u.blk0 + kBpt * jj));
       if (ok && !*sh.abort_flag) {
         const uint32_t vb = sh.base + C::kOffV + s * C::kTileBytes;
         for (int kk = 0; kk < nbk; ++kk) {
@@ -227,9 +233,10 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
         const uint32_t kb = sh.base + C::kOffK + s * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          ptx::mma_bf16(tmem + sb * kTileTok, ptx::sdesc_sw128(qb + off, 16, 1024),
-                        ptx::sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t qoff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * (kTileTok * 128) + (kk & 3) * 32;
+          ptx::mma_bf16(tmem + sb * kTileTok, ptx::sdesc_sw128(qb + qoff, 16, 1024),
+                        ptx::sdesc_sw128(kb + koff, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
         }
         issued = true;
       }
@@ -256,9 +263,8 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 }
 
 template <int D>
-__device__ void write_row_out(const AttnParams& p, const UnitDesc& u, int grow, const float* o,
-                              float inv, float lse2) {
-  const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
+__device__ void write_row_out(const AttnParams& p, const UnitDesc& u, int grow, const GroupTok& gt,
+                              const float* o, float inv, float lse2) {
   const int h = u.kvh * p.gqa + grow % p.gqa;
   float* dst;
   if (gt.pbase < 0) {
@@ -375,12 +381,12 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
     const int s = (g + j) % C::kStages;
     const bool ok = __all_sync(
         0xffffffffu, wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns));
-    const int nb = min(8, u.blk1 - (u.blk0 + 8 * j));
+    const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
     const uint8_t* kst = sh.ptr + C::kOffK + s * C::kTileBytes + half * (kTileTok * 128) + inb;
     const uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes + half * (kTileTok * 128) + inb;
     if (ok) {
       for (int bb = warp; bb < nb; bb += 4) {
-        const int mt = sh.meta[s * 8 + bb];
+        const int mt = sh.meta[s * kBpt + bb];
         const int pos = mt >> 5, nvalid = mt & 31;
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
@@ -427,8 +433,8 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
     if (tid == 0) ptx::mbar_arrive(B.empty(s));
   }
   // combine the four warps' states (scratch in the P buffer, idle here)
-  float* sm_o = reinterpret_cast<float*>(sh.ptr + C::kOffP);  // [4][RB][D]
-  float* sm_ml = sm_o + 4 * RB * D;                            // [4][RB][2]
+  float* sm_o = reinterpret_cast<float*>(sh.ptr + C::kOffP);   // [4][RB][D]
+  float* sm_ml = reinterpret_cast<float*>(sh.ptr + C::kOffML);  // [4][RB][2]
 #pragma unroll
   for (int i = 0; i < RB; ++i) {
     if (lane == 0) {
@@ -488,25 +494,25 @@ __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1)
 
 // Start copying unit k's query tile (row tid; zeros past its rows) into the
 // swizzled buffer at qb.  Completion: cp_async_wait_all().
-// Returns the row's visible end in the group span (0 past the unit's rows).
+// Returns the row's record (token, visible end, partial slot); vis = 0 past
+// the unit's rows.
 template <int D>
-__device__ __forceinline__ int prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
+__device__ __forceinline__ GroupTok prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
   const UnitDesc u = p.units[k];
   const bool row_ok = tid < u.nrows;
   const uint16_t* src = p.q;
-  int vis = 0;
+  GroupTok gt{0, 0, -1, 0};
   if (row_ok) {
     const int grow = u.row0 + tid;
-    const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
+    gt = p.gtoks[u.tok_off + grow / p.gqa];
     const int h = u.kvh * p.gqa + grow % p.gqa;
     src = p.q + ((size_t)gt.tok * p.hq + h) * D;
-    vis = gt.vis;
   }
 #pragma unroll
   for (int c = 0; c < D / 8; ++c)
     ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), src + c * 8, row_ok ? 16u : 0u);
   ptx::cp_async_commit();
-  return vis;
+  return gt;
 }
 
 template <int D>
@@ -518,12 +524,12 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   const uint32_t qbuf0 = sh.base + C::kOffQ;
   uint32_t g = 0, gm = 0, nu = 0;
-  int vis_next = 0;  // visible end of this thread's row in the next tensor-core unit
+  GroupTok gt_next{0, 0, -1, 0};  // this thread's row record in the next tensor-core unit
   // the first tensor-core unit's query tile, before anything else
   {
     const int first = next_mma_unit(p, u0, u1);
     if (first >= 0) {
-      vis_next = prefetch_q<D>(p, first, qbuf0, tid);
+      gt_next = prefetch_q<D>(p, first, qbuf0, tid);
       ptx::cp_async_wait_all();
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(B.q_full(0));
@@ -539,7 +545,8 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         float z[D];
 #pragma unroll
         for (int c = 0; c < D; ++c) z[c] = 0.f;
-        write_row_out<D>(p, u, u.row0 + tid, z, 0.f, -INFINITY);
+        const GroupTok gt = p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa];
+        write_row_out<D>(p, u, u.row0 + tid, gt, z, 0.f, -INFINITY);
       }
       continue;
     }
@@ -550,9 +557,10 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     }
     // The next tensor-core unit's query tile streams into the other buffer
     // while this unit runs (its previous user finished before our epilogue).
-    const int vis = vis_next;
+    const GroupTok gt_row = gt_next;
+    const int vis = gt_row.vis;
     const int nxt = next_mma_unit(p, ui + 1, u1);
-    if (nxt >= 0) vis_next = prefetch_q<D>(p, nxt, qbuf0 + ((nu + 1) & 1) * C::kQBytes, tid);
+    if (nxt >= 0) gt_next = prefetch_q<D>(p, nxt, qbuf0 + ((nu + 1) & 1) * C::kQBytes, tid);
 
     const bool row_ok = tid < u.nrows;
     const bool wact = warp * 32 < u.nrows;  // warps of padding rows only keep the barriers in step
@@ -565,14 +573,14 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       ok = ok && wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
-      const int nb = min(8, u.blk1 - (u.blk0 + 8 * j));
-      int lim[8];
+      const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
+      int lim[kBpt];
       bool partial = false;
 #pragma unroll
-      for (int bb = 0; bb < 8; ++bb) {
+      for (int bb = 0; bb < kBpt; ++bb) {
         lim[bb] = 0;
         if (bb < nb) {
-          const int mt = sh.meta[s * 8 + bb];
+          const int mt = sh.meta[s * kBpt + bb];
           const int pos = mt >> 5, nvalid = mt & 31;
           partial |= nvalid < 16;
           if (row_ok) lim[bb] = max(0, min(nvalid, vis - pos));
@@ -599,8 +607,8 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTileTok; ++c)
-        if ((c & 15) < lim[c >> 4]) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+      for (int c = 0; c < kTileTok; ++c)  // branch-free: masked scores select -inf
+        mx8[c & 7] = fmaxf(mx8[c & 7], (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY);
       const float mx =
           fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
@@ -616,9 +624,12 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       if (wact) {
 #pragma unroll
         for (int c = 0; c < kTileTok; c += 2) {
-          const float a = ((c & 15) < lim[c >> 4]) ? ptx::ex2(fmaf(sv[c], p.scale_log2, -m_new)) : 0.f;
-          const float b = (((c + 1) & 15) < lim[(c + 1) >> 4])
-                              ? ptx::ex2(fmaf(sv[c + 1], p.scale_log2, -m_new)) : 0.f;
+          // masked slots take exp2(-inf) = 0 (a select, not a branch)
+          const float xa = (c & 15) < lim[c >> 4] ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY;
+          const float xb =
+              ((c + 1) & 15) < lim[(c + 1) >> 4] ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY;
+          const float a = ptx::ex2(xa);
+          const float b = ptx::ex2(xb);
           pk[c >> 1] = ptx::pack_bf16(a, b);
           ps4[(c >> 1) & 3] += bf16_lo(pk[c >> 1]) + bf16_hi(pk[c >> 1]);
           pe4[(c >> 1) & 3] += a + b;
@@ -656,7 +667,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes;
         for (int idx = tid; idx < nb * 16 * C::kHalves * 8; idx += kComputeThreads) {
           const int ch = idx & 7, r = (idx >> 3) % (nb * 16), hh = (idx >> 3) / (nb * 16);
-          const int nvalid = sh.meta[s * 8 + (r >> 4)] & 31;
+          const int nvalid = sh.meta[s * kBpt + (r >> 4)] & 31;
           if ((r & 15) >= nvalid)
             *reinterpret_cast<uint4*>(vst + hh * (kTileTok * 128) + r * 128 + ch * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -690,7 +701,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       if (row_ok && !*sh.abort_flag) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const float lse2 = l_exact > 0.f ? m_run + __log2f(l_exact) : -INFINITY;
-        write_row_out<D>(p, u, u.row0 + tid, o, inv, lse2);
+        write_row_out<D>(p, u, u.row0 + tid, gt_row, o, inv, lse2);
       }
     }
     ptx::tc_fence_before();
@@ -735,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(B.q_full(1), kComputeThreads);
     ptx::mbar_init(B.o_full(), 1);
     ptx::mbar_init(B.drain(), 1);
+    ptx::mbar_init(B.never(), 1);  // nothing arrives here
     *sh.abort_flag = 0;
     ptx::fence_mbar_init();
   }
