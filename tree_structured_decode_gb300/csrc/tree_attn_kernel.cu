@@ -39,10 +39,17 @@
 namespace ta {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kComputeThreads = 128;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+// Three warpgroups: two compute (threads i and i+128 share row i), and one
+// holding the TMA producer warp, the tcgen05 issuer warp and two idle warps.
+// The launch gives every thread 168 registers; the roles then rebalance to
+// 216 (compute) and 64 (producer/issuer): 256 x 216 + 128 x 64 <= 384 x 168.
+constexpr int kThreads = 384;
+constexpr int kComputeThreads = 256;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kComputeRegs = 216;
+constexpr int kIssueRegs = 64;
+static_assert(256 * kComputeRegs + 128 * kIssueRegs <= kThreads * 168, "register split too large");
 constexpr int kTileTok = kKvTileTokens;  // KV tokens per tile (4 pages)
 constexpr int kBpt = kTileTok / 16;       // pages (blocks) per tile
 constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
@@ -53,7 +60,7 @@ constexpr long long kDrainLimitNs = 200000000;  // 200 ms for copies / MMAs alre
 template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kStages = D == 128 ? 3 : 8;
   static constexpr int kQBytes = 128 * D * 2;          // one query tile
   static constexpr int kTileBytes = kTileTok * D * 2;  // K (or V) of one tile
   static constexpr int kPBytes = 128 * kTileTok * 2;
@@ -61,13 +68,19 @@ struct Cfg {
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
-  static constexpr int kNumBars = 2 * kStages + 11;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;  // two P buffers
+  static constexpr int kNumBars = 2 * kStages + 12;
   static constexpr int kOffMeta = kOffBar + kNumBars * 8 + 16;     // int [kStages][kBpt]
   static constexpr int kOffML = kOffMeta + kStages * kBpt * 4;      // float [4][8][2]
-  static constexpr int kSmem = kOffML + 4 * kSimtTileRows * 2 * 4 + 1024;  // + alignment slack
+  static constexpr int kOffXM = kOffML + 4 * kSimtTileRows * 2 * 4;  // float [2][2][128] row max
+  static constexpr int kOffXL = kOffXM + 2 * 2 * 128 * 4;            // float [2][128][2] row sums
+  static constexpr int kSmem = kOffXL + 2 * 128 * 2 * 4 + 1024;      // + alignment slack
   // the CUDA-core path combines its four warps' O in the (idle) P buffer
   static_assert(4 * kSimtTileRows * D * 4 <= kPBytes, "combine scratch exceeds the P buffer");
+  // A stage holds K as [64-column half][tile token][128 B] (one box per page
+  // and half; QK^T is one N = kTileTok MMA per 16 columns of d) and V as
+  // [page][64-column half][16 tokens][128 B] (one box per page-head; P.V is
+  // one MMA per page).  Both 128-byte swizzled.
   static constexpr uint32_t kBlockBytes = 16 * D * 2;                // one page-head
   static constexpr uint32_t kIdescQK = ptx::idesc_bf16(128, kTileTok, 0);
   static constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, D, 1);
@@ -89,7 +102,7 @@ struct Bars {
   __device__ uint32_t s_full(int i) const { return b + 8 * (2 * Cfg<D>::kStages + i); }
   __device__ uint32_t s_free(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 2 + i); }
   __device__ uint32_t p_full() const { return b + 8 * (2 * Cfg<D>::kStages + 4); }
-  __device__ uint32_t p_empty() const { return b + 8 * (2 * Cfg<D>::kStages + 5); }
+  __device__ uint32_t p_empty(int i) const { return b + 8 * (2 * Cfg<D>::kStages + (i ? 11 : 5)); }
   __device__ uint32_t o_full() const { return b + 8 * (2 * Cfg<D>::kStages + 6); }
   __device__ uint32_t drain() const { return b + 8 * (2 * Cfg<D>::kStages + 7); }
   __device__ uint32_t q_full(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 8 + i); }
@@ -164,11 +177,13 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
       for (int bb = 0; bb < kBpt; ++bb) {
         if (bb < nb) {
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            const uint32_t off = h * (kTileTok * 128) + bb * (16 * 128);
-            ptx::tma_load_4d(kdst + off, tmk, 64 * h, 0, u.kvh, bl[bb].x, B.full(s));
-            ptx::tma_load_4d(vdst + off, tmv, 64 * h, 0, u.kvh, bl[bb].x, B.full(s));
-          }
+          for (int h = 0; h < C::kHalves; ++h)
+            ptx::tma_load_4d(kdst + h * (kTileTok * 128) + bb * 2048, tmk, 64 * h, 0, u.kvh,
+                             bl[bb].x, B.full(s));
+          if constexpr (D == 128)  // both 64-column halves of V in one box
+            ptx::tma_load_5d(vdst + bb * C::kBlockBytes, tmv, 0, 0, 0, u.kvh, bl[bb].x, B.full(s));
+          else
+            ptx::tma_load_4d(vdst + bb * C::kBlockBytes, tmv, 0, 0, u.kvh, bl[bb].x, B.full(s));
         }
       }
 #pragma unroll
@@ -213,15 +228,16 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       const int nbk = min(kBpt, u.blk1 - (u.blk0 + kBpt * jj));
       if (ok && !*sh.abort_flag) {
         const uint32_t vb = sh.base + C::kOffV + s * C::kTileBytes;
+        const uint32_t pb = pbase + ((gm + jj) & 1) * C::kPBytes;
         for (int kk = 0; kk < nbk; ++kk) {
-          const uint64_t ad = ptx::sdesc_sw128(pbase + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(vb + kk * 2048, kTileTok * 128, 1024);
+          const uint64_t ad = ptx::sdesc_sw128(pb + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(vb + kk * C::kBlockBytes, 2048, 1024);
           ptx::mma_bf16(o_tmem, ad, bd, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         issued = true;
       }
       ptx::mma_commit(B.empty(s));
-      ptx::mma_commit(B.p_empty());
+      ptx::mma_commit(B.p_empty((gm + jj) & 1));
     };
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
@@ -260,25 +276,6 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
 // swizzled half) for 8-element chunk granularity.
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
-template <int D>
-__device__ void write_row_out(const AttnParams& p, const UnitDesc& u, int grow, const GroupTok& gt,
-                              const float* o, float inv, float lse2) {
-  const int h = u.kvh * p.gqa + grow % p.gqa;
-  float* dst;
-  if (gt.pbase < 0) {
-    dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
-    if (p.lse) p.lse[(size_t)gt.tok * p.hq + h] = lse2 * kLn2;
-  } else {
-    const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
-    dst = p.part_o + slot * D;
-    p.part_lse[slot] = lse2;
-  }
-#pragma unroll
-  for (int c = 0; c < D; c += 4)
-    *reinterpret_cast<float4*>(dst + c) =
-        make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
 }
 
 template <int EPL>
@@ -383,7 +380,7 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
         0xffffffffu, wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns));
     const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
     const uint8_t* kst = sh.ptr + C::kOffK + s * C::kTileBytes + half * (kTileTok * 128) + inb;
-    const uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes + half * (kTileTok * 128) + inb;
+    const uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes + half * 2048 + inb;
     if (ok) {
       for (int bb = warp; bb < nb; bb += 4) {
         const int mt = sh.meta[s * kBpt + bb];
@@ -422,7 +419,7 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
           for (int t = 0; t < lim; ++t) {
             const float pt = __shfl_sync(0xffffffffu, pl, 2 * t);
             float vf[EPL];
-            load_slice<EPL>(vst + sw128(bb * 16 + t, chunk), vf);
+            load_slice<EPL>(vst + bb * C::kBlockBytes + sw128(t, chunk), vf);
 #pragma unroll
             for (int e = 0; e < EPL; ++e) o[i][e] = fmaf(pt, vf[e], o[i][e]);
           }
@@ -435,17 +432,19 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
   // combine the four warps' states (scratch in the P buffer, idle here)
   float* sm_o = reinterpret_cast<float*>(sh.ptr + C::kOffP);   // [4][RB][D]
   float* sm_ml = reinterpret_cast<float*>(sh.ptr + C::kOffML);  // [4][RB][2]
+  if (warp < 4) {  // only warps 0-3 take blocks (4 per tile); 4-7 help write rows
 #pragma unroll
-  for (int i = 0; i < RB; ++i) {
-    if (lane == 0) {
-      sm_ml[(warp * RB + i) * 2 + 0] = m[i];
-      sm_ml[(warp * RB + i) * 2 + 1] = l[i];
+    for (int i = 0; i < RB; ++i) {
+      if (lane == 0) {
+        sm_ml[(warp * RB + i) * 2 + 0] = m[i];
+        sm_ml[(warp * RB + i) * 2 + 1] = l[i];
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) sm_o[(warp * RB + i) * D + lane * EPL + e] = o[i][e];
     }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) sm_o[(warp * RB + i) * D + lane * EPL + e] = o[i][e];
   }
   ptx::named_bar_sync(1, kComputeThreads);
-  for (int i = warp; i < nr; i += 4) {
+  for (int i = warp; i < nr; i += kComputeThreads / 32) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 4; ++w) M = fmaxf(M, sm_ml[(w * RB + i) * 2]);
@@ -492,37 +491,72 @@ __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1)
   return -1;
 }
 
-// Start copying unit k's query tile (row tid; zeros past its rows) into the
-// swizzled buffer at qb.  Completion: cp_async_wait_all().
-// Returns the row's record (token, visible end, partial slot); vis = 0 past
-// the unit's rows.
+// Start copying unit k's query tile into the swizzled buffer at qb: row
+// tid & 127, this warpgroup's half of its 16-byte chunks (zeros past the unit's
+// rows).  Completion: cp_async_wait_all().  Returns the row's record (token,
+// visible end, partial slot); vis = 0 past the unit's rows.
 template <int D>
 __device__ __forceinline__ GroupTok prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
   const UnitDesc u = p.units[k];
-  const bool row_ok = tid < u.nrows;
+  const int row = tid & 127, wg = tid >> 7;
+  const bool row_ok = row < u.nrows;
   const uint16_t* src = p.q;
   GroupTok gt{0, 0, -1, 0};
   if (row_ok) {
-    const int grow = u.row0 + tid;
+    const int grow = u.row0 + row;
     gt = p.gtoks[u.tok_off + grow / p.gqa];
     const int h = u.kvh * p.gqa + grow % p.gqa;
     src = p.q + ((size_t)gt.tok * p.hq + h) * D;
   }
+  constexpr int kHalf = D / 16;  // chunks per warpgroup
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c)
-    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), src + c * 8, row_ok ? 16u : 0u);
+  for (int cc = 0; cc < kHalf; ++cc) {
+    const int c = wg * kHalf + cc;
+    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(row, c & 7), src + c * 8, row_ok ? 16u : 0u);
+  }
   ptx::cp_async_commit();
   return gt;
 }
 
+// Write columns [c0, c0 + n) of row `grow`'s result (normalised O, and lse
+// when with_lse) to the output or to its partial slot.
+template <int D, int N>
+__device__ __forceinline__ void write_row_cols(const AttnParams& p, const UnitDesc& u, int grow,
+                                               const GroupTok& gt, const float* o, int c0, float inv,
+                                               float lse2, bool with_lse) {
+  const int h = u.kvh * p.gqa + grow % p.gqa;
+  float* dst;
+  if (gt.pbase < 0) {
+    dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
+    if (with_lse && p.lse) p.lse[(size_t)gt.tok * p.hq + h] = lse2 * kLn2;
+  } else {
+    const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
+    dst = p.part_o + slot * D;
+    if (with_lse) p.part_lse[slot] = lse2;
+  }
+#pragma unroll
+  for (int c = 0; c < N; c += 4)
+    *reinterpret_cast<float4*>(dst + c0 + c) =
+        make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+}
+
+// The eight compute warps.  Tensor-core units: thread i < 128 and thread
+// i + 128 own TMEM lane (row) i together and split every tile's columns and
+// O's columns between them; they exchange one partial row max per tile
+// through shared memory.  CUDA-core units: see simt_unit.
 template <int D>
 __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared& sh,
                               const Bars<D>& B, uint32_t tmem) {
   using C = Cfg<D>;
-  const int tid = threadIdx.x;  // query row within the tile / TMEM lane
+  constexpr int kCols = kTileTok / 2;  // tile columns per thread
+  constexpr int kOCols = D / 2;        // O columns per thread
+  const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const int row = tid & 127, wg = tid >> 7;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t qbuf0 = sh.base + C::kOffQ;
+  float* xmax = reinterpret_cast<float*>(sh.ptr + C::kOffXM);  // [2 bufs][2 wg][128]
+  float* xl = reinterpret_cast<float*>(sh.ptr + C::kOffXL);    // [2 wg][128][2]
   uint32_t g = 0, gm = 0, nu = 0;
   GroupTok gt_next{0, 0, -1, 0};  // this thread's row record in the next tensor-core unit
   // the first tensor-core unit's query tile, before anything else
@@ -542,11 +576,20 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     const int T = unit_tiles(u);
     if (T == 0) {  // empty span: every row sees nothing
       if (tid < u.nrows && !*sh.abort_flag) {
-        float z[D];
-#pragma unroll
-        for (int c = 0; c < D; ++c) z[c] = 0.f;
-        const GroupTok gt = p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa];
-        write_row_out<D>(p, u, u.row0 + tid, gt, z, 0.f, -INFINITY);
+        const int grow = u.row0 + tid;
+        const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
+        const int h = u.kvh * p.gqa + grow % p.gqa;
+        float* dst;
+        if (gt.pbase < 0) {
+          dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
+          if (p.lse) p.lse[(size_t)gt.tok * p.hq + h] = -INFINITY;
+        } else {
+          const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
+          dst = p.part_o + slot * D;
+          p.part_lse[slot] = -INFINITY;
+        }
+        for (int c = 0; c < D; c += 4)
+          *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       continue;
     }
@@ -562,9 +605,9 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     const int nxt = next_mma_unit(p, ui + 1, u1);
     if (nxt >= 0) gt_next = prefetch_q<D>(p, nxt, qbuf0 + ((nu + 1) & 1) * C::kQBytes, tid);
 
-    const bool row_ok = tid < u.nrows;
-    const bool wact = warp * 32 < u.nrows;  // warps of padding rows only keep the barriers in step
-    const uint32_t o_tmem = tmem + lane_base + 256 + (nu & 1) * 128;
+    const bool row_ok = row < u.nrows;
+    const bool wact = (warp & 3) * 32 < u.nrows;  // warps of padding rows keep the barriers only
+    const uint32_t o_tmem = tmem + lane_base + 256 + (nu & 1) * 128 + wg * kOCols;
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
@@ -574,44 +617,48 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
       const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
-      int lim[kBpt];
+      // visible slots of this thread's two blocks (columns wg*32 .. wg*32+31)
+      int lim[2];
       bool partial = false;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
-        lim[bb] = 0;
         if (bb < nb) {
           const int mt = sh.meta[s * kBpt + bb];
-          const int pos = mt >> 5, nvalid = mt & 31;
-          partial |= nvalid < 16;
-          if (row_ok) lim[bb] = max(0, min(nvalid, vis - pos));
+          partial |= (mt & 31) < 16;
+          if ((bb >> 1) == wg) lim[bb & 1] = row_ok ? max(0, min(mt & 31, vis - (mt >> 5))) : 0;
+        } else if ((bb >> 1) == wg) {
+          lim[bb & 1] = 0;
         }
       }
-      float sv[kTileTok];
+      float sv[kCols];
       if (ok && wact) {
-#pragma unroll
-        for (int c = 0; c < kTileTok / 32; ++c) {
-          float t32[32];
-          ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + c * 32, t32);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t32[e];
-        }
+        float t32[32];
+        ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + wg * kCols, t32);
         ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) sv[e] = t32[e];
       } else {
 #pragma unroll
-        for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
+        for (int e = 0; e < kCols; ++e) sv[e] = 0.f;
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(B.s_free(sb));
-      // masked row max, eight independent chains (scores in log2 units)
+      // masked partial row max, eight independent chains; masked scores
+      // select -inf (a select, not a branch)
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kTileTok; ++c)  // branch-free: masked scores select -inf
+      for (int c = 0; c < kCols; ++c)
         mx8[c & 7] = fmaxf(mx8[c & 7], (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY);
-      const float mx =
-          fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // the other half of the row (double-buffered: a slow partner can still
+      // read this tile's value while we write the next tile's)
+      float* xm = xmax + ((gm + j) & 1) * 256;
+      xm[wg * 128 + row] = mx;
+      ptx::named_bar_sync(2, kComputeThreads);
+      mx = fmaxf(mx, xm[(wg ^ 1) * 128 + row]) * p.scale_log2;
       float m_new = m_run, alpha = 1.f;
       if (wact && mx > m_run + kRescaleLog2) {
         m_new = mx;
@@ -619,12 +666,11 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       }
       // P rounds to bf16 for the tensor cores; O is normalised by the sum of
       // the rounded weights (the weights the MMA used), lse by the exact sum.
-      uint32_t pk[kTileTok / 2];
+      uint32_t pk[kCols / 2];
       float ps4[4] = {0.f, 0.f, 0.f, 0.f}, pe4[4] = {0.f, 0.f, 0.f, 0.f};
       if (wact) {
 #pragma unroll
-        for (int c = 0; c < kTileTok; c += 2) {
-          // masked slots take exp2(-inf) = 0 (a select, not a branch)
+        for (int c = 0; c < kCols; c += 2) {
           const float xa = (c & 15) < lim[c >> 4] ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY;
           const float xb =
               ((c + 1) & 15) < lim[(c + 1) >> 4] ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY;
@@ -638,13 +684,18 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       l_run = fmaf(l_run, alpha, (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
       l_exact = fmaf(l_exact, alpha, (pe4[0] + pe4[1]) + (pe4[2] + pe4[3]));
       m_run = m_new;
-      // P buffer and O are free once the previous P.V has completed
-      ok = wait_bar(B.p_empty(), (gm + j + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
+      // P buffer n & 1 is free once P.V of tile n - 2 has completed; O may
+      // be rescaled only after P.V of tile n - 1
+      const uint32_t n = gm + j;
+      ok = wait_bar(B.p_empty(n & 1), ((n >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
       ok = __all_sync(0xffffffffu, ok);
+      const bool resc = ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+      if (resc) ok = __all_sync(0xffffffffu, wait_bar(B.p_empty((n - 1) & 1), ((n - 1) >> 1) & 1, sh,
+                                                        p.err, p.wait_timeout_ns));
       ptx::tc_fence_after();
-      if (ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (resc && ok) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kOCols / 32; ++c) {
           float t32[32];
           ptx::tmem_ld32(o_tmem + c * 32, t32);
           ptx::tmem_wait_ld();
@@ -655,10 +706,10 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         ptx::tmem_wait_st();
       }
       if (wact) {
-        const uint32_t pb = sh.base + C::kOffP;
+        const uint32_t pb = sh.base + C::kOffP + (n & 1) * C::kPBytes;
 #pragma unroll
-        for (int c = 0; c < kTileTok / 8; ++c)
-          ptx::st_shared_v4(pb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), pk[4 * c], pk[4 * c + 1],
+        for (int c = 0; c < kCols / 8; ++c)
+          ptx::st_shared_v4(pb + sw128(row, wg * (kCols / 8) + c), pk[4 * c], pk[4 * c + 1],
                             pk[4 * c + 2], pk[4 * c + 3]);
       }
       if (partial) {
@@ -669,7 +720,8 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
           const int ch = idx & 7, r = (idx >> 3) % (nb * 16), hh = (idx >> 3) / (nb * 16);
           const int nvalid = sh.meta[s * kBpt + (r >> 4)] & 31;
           if ((r & 15) >= nvalid)
-            *reinterpret_cast<uint4*>(vst + hh * (kTileTok * 128) + r * 128 + ch * 16) =
+            *reinterpret_cast<uint4*>(vst + (r >> 4) * C::kBlockBytes + hh * 2048 + (r & 15) * 128 +
+                                      ch * 16) =
                 make_uint4(0, 0, 0, 0);
         }
       }
@@ -684,14 +736,19 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(B.q_full((nu + 1) & 1));
     }
-    // ---- epilogue: O / l
+    // ---- epilogue: O / l, row sums combined across the two halves
+    xl[(wg * 128 + row) * 2 + 0] = l_run;
+    xl[(wg * 128 + row) * 2 + 1] = l_exact;
+    ptx::named_bar_sync(2, kComputeThreads);
+    l_run += xl[((wg ^ 1) * 128 + row) * 2 + 0];
+    l_exact += xl[((wg ^ 1) * 128 + row) * 2 + 1];
     bool ok = wait_bar(B.o_full(), nu & 1, sh, p.err, p.wait_timeout_ns);
     ok = __all_sync(0xffffffffu, ok);
     ptx::tc_fence_after();
     if (ok && wact) {
-      float o[D];
+      float o[kOCols];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kOCols / 32; ++c) {
         float t32[32];
         ptx::tmem_ld32(o_tmem + c * 32, t32);
 #pragma unroll
@@ -701,7 +758,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       if (row_ok && !*sh.abort_flag) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         const float lse2 = l_exact > 0.f ? m_run + __log2f(l_exact) : -INFINITY;
-        write_row_out<D>(p, u, u.row0 + tid, gt_row, o, inv, lse2);
+        write_row_cols<D, kOCols>(p, u, u.row0 + row, gt_row, o, wg * kOCols, inv, lse2, wg == 0);
       }
     }
     ptx::tc_fence_before();
@@ -741,7 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(B.s_free(i), kComputeThreads);
     }
     ptx::mbar_init(B.p_full(), kComputeThreads);
-    ptx::mbar_init(B.p_empty(), 1);
+    ptx::mbar_init(B.p_empty(0), 1);
+    ptx::mbar_init(B.p_empty(1), 1);
     ptx::mbar_init(B.q_full(0), kComputeThreads);
     ptx::mbar_init(B.q_full(1), kComputeThreads);
     ptx::mbar_init(B.o_full(), 1);
@@ -771,13 +829,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *sh.tmem_slot;
 
-  if (warp < 4) {
+  if (warp < kComputeThreads / 32) {
+    ptx::setmaxnreg_inc<kComputeRegs>();
     compute_warps<D>(p, u0, u1, sh, B, tmem);
-  } else if (warp == kProducerWarp) {
-    if (lane == 0) producer<D>(&tmk, &tmv, p, u0, u1, sh, B);
-    __syncwarp();
   } else {
-    if (lane == 0) mma_issuer<D>(p, u0, u1, sh, B, tmem);
+    ptx::setmaxnreg_dec<kIssueRegs>();
+    if (warp == kProducerWarp) {
+      if (lane == 0) producer<D>(&tmk, &tmv, p, u0, u1, sh, B);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) mma_issuer<D>(p, u0, u1, sh, B, tmem);
+    }  // warps 10 and 11 only complete the warpgroup
     __syncwarp();
   }
   ptx::tc_fence_before();
@@ -803,18 +864,34 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Page pool [pages][hkv][16][d] bf16 as a 4-D tensor (d, slot, head, page);
-// one box = one 64-column half of one page-head, 128-byte swizzle.
-cudaError_t make_page_map(CUtensorMap* m, const void* base, int d, int hkv, int num_pages) {
+// Page pool [pages][hkv][16][d] bf16 as a 4-D tensor (d, slot, head, page)
+// whose box is one 64-column half of a page-head; or, for whole_page_head
+// with d = 128, a 5-D tensor (64 columns, slot, column half, head, page) whose
+// half dimension (stride 128 B) sits outside the slot dimension (stride
+// 256 B), so one box lands a whole page-head as [half][16 slots][64 columns].
+// 128-byte swizzle in both cases.
+cudaError_t make_page_map(CUtensorMap* m, const void* base, int d, int hkv, int num_pages,
+                          bool whole_page_head) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[4] = {(cuuint64_t)d, 16, (cuuint64_t)hkv, (cuuint64_t)num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)16 * d * 2, (cuuint64_t)hkv * 16 * d * 2};
-  cuuint32_t box[4] = {64, 16, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (d == 128 && whole_page_head) {
+    cuuint64_t dims[5] = {64, 16, 2, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[4] = {256, 128, 4096, (cuuint64_t)hkv * 4096};
+    cuuint32_t box[5] = {64, 16, 2, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[4] = {(cuuint64_t)d, 16, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)16 * d * 2, (cuuint64_t)hkv * 16 * d * 2};
+    cuuint32_t box[4] = {64, 16, 1, 1};  // one 64-column half of a page-head
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -831,9 +908,9 @@ cudaError_t launch_d(const AttnParams& p, int grid, int num_pages, cudaStream_t 
   memset(&mk, 0, sizeof mk);
   memset(&mv, 0, sizeof mv);
   if (num_pages > 0) {
-    cudaError_t e = make_page_map(&mk, p.k, D, p.hkv, num_pages);
+    cudaError_t e = make_page_map(&mk, p.k, D, p.hkv, num_pages, false);
     if (e != cudaSuccess) return e;
-    e = make_page_map(&mv, p.v, D, p.hkv, num_pages);
+    e = make_page_map(&mv, p.v, D, p.hkv, num_pages, true);
     if (e != cudaSuccess) return e;
   }
   tree_attn_kernel<D><<<grid, kThreads, Cfg<D>::kSmem, s>>>(mk, mv, p);
