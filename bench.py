@@ -258,7 +258,7 @@ def bench_ours(args, rank, world, local):
                 "frac": round(tf / tc_peak, 4)}
     roof["peak_source"] = peak_kind
     roof["traffic"] = committed_traffic(
-        os.path.join(ROOT, "tree_structured_decode_gb300", "csrc", "attn_kernels.cu"),
+        os.path.join(ROOT, "tree_structured_decode_gb300", "csrc", "tree_attn_kernel.cu"),
         args.workload)
     roof["kernel"] = "partial attention pass"
     roof["kernel_ms"] = round(t_part, 5)
