@@ -362,7 +362,7 @@ tree_attn_status build_host_plan(
         }
   }
   const int64_t nu = (int64_t)p.units.size();
-  p.grid = (int32_t)std::min<int64_t>(nu, std::max(1, opt.num_sms));
+  p.grid = (int32_t)std::min<int64_t>(nu, (int64_t)std::max(1, opt.num_sms) * kCtasPerSm);
   {
     std::vector<int32_t> order(nu);
     for (int64_t i = 0; i < nu; ++i) order[i] = (int32_t)i;

@@ -22,6 +22,7 @@ constexpr int kKvTileTokens = 64;                  // one KV tile = 4 pages
 constexpr int kBlocksPerTile = kKvTileTokens / kPageSize;
 constexpr int kMmaTileRows = 128;                  // tcgen05 M
 constexpr int kSimtTileRows = 8;                   // CUDA-core rows per unit
+constexpr int kCtasPerSm = 2;                      // co-resident persistent CTAs per SM
 constexpr int kPathSimt = 0;
 constexpr int kPathMma = 1;
 

@@ -39,42 +39,44 @@
 namespace ta {
 namespace {
 
-// Three warpgroups: two compute (threads i and i+128 share row i), and one
-// holding the TMA producer warp, the tcgen05 issuer warp and two idle warps.
-// The launch gives every thread 168 registers; the roles then rebalance to
-// 216 (compute) and 64 (producer/issuer): 256 x 216 + 128 x 64 <= 384 x 168.
-constexpr int kThreads = 384;
-constexpr int kComputeThreads = 256;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kComputeRegs = 216;
-constexpr int kIssueRegs = 64;
-static_assert(256 * kComputeRegs + 128 * kIssueRegs <= kThreads * 168, "register split too large");
+// Two CTAs per SM, each a full pipeline of two warpgroups: four compute warps
+// (thread i owns TMEM lane / query row i) and one warpgroup holding the TMA
+// producer warp, the tcgen05 issuer warp and two idle warps.  The launch gives
+// every thread 128 registers; the roles rebalance to 200 (compute) and 56
+// (producer/issuer): 128 x 200 + 128 x 56 <= 256 x 128.  The second CTA on
+// the SM fills the latency gaps of the first.
+constexpr int kThreads = 256;
+constexpr int kComputeThreads = 128;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kComputeRegs = 200;
+constexpr int kIssueRegs = 56;
+static_assert(128 * kComputeRegs + 128 * kIssueRegs <= kThreads * 128, "register split too large");
 constexpr int kTileTok = kKvTileTokens;  // KV tokens per tile (4 pages)
 constexpr int kBpt = kTileTok / 16;       // pages (blocks) per tile
 constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 256;  // S0, S1 (64 columns each) and O (128)
 constexpr long long kDrainLimitNs = 200000000;  // 200 ms for copies / MMAs already in flight
 
 template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = D == 128 ? 3 : 8;
-  static constexpr int kQBytes = 128 * D * 2;          // one query tile
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kQBytes = 128 * D * 2;          // the query tile
   static constexpr int kTileBytes = kTileTok * D * 2;  // K (or V) of one tile
   static constexpr int kPBytes = 128 * kTileTok * 2;
-  static constexpr int kOffQ = 0;                      // two query tiles
-  static constexpr int kOffK = kOffQ + 2 * kQBytes;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;  // two P buffers
-  static constexpr int kNumBars = 2 * kStages + 12;
+  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kNumBars = 2 * kStages + 13;
   static constexpr int kOffMeta = kOffBar + kNumBars * 8 + 16;     // int [kStages][kBpt]
   static constexpr int kOffML = kOffMeta + kStages * kBpt * 4;      // float [4][8][2]
-  static constexpr int kOffXM = kOffML + 4 * kSimtTileRows * 2 * 4;  // float [2][2][128] row max
-  static constexpr int kOffXL = kOffXM + 2 * 2 * 128 * 4;            // float [2][128][2] row sums
-  static constexpr int kSmem = kOffXL + 2 * 128 * 2 * 4 + 1024;      // + alignment slack
+  // the dynamic shared window starts 1024-byte aligned (checked at start)
+  static constexpr int kSmem = kOffML + 4 * kSimtTileRows * 2 * 4;
+  static_assert(kSmem <= 115 * 1024, "two CTAs per SM must fit in shared memory");
   // the CUDA-core path combines its four warps' O in the (idle) P buffer
   static_assert(4 * kSimtTileRows * D * 4 <= kPBytes, "combine scratch exceeds the P buffer");
   // A stage holds K as [64-column half][tile token][128 B] (one box per page
@@ -107,6 +109,7 @@ struct Bars {
   __device__ uint32_t drain() const { return b + 8 * (2 * Cfg<D>::kStages + 7); }
   __device__ uint32_t q_full(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 8 + i); }
   __device__ uint32_t never() const { return b + 8 * (2 * Cfg<D>::kStages + 10); }
+  __device__ uint32_t o_empty() const { return b + 8 * (2 * Cfg<D>::kStages + 12); }
 };
 
 // Bounded wait.  Returns false (and does not wait) once the CTA has aborted;
@@ -217,18 +220,21 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       g += T;
       continue;
     }
-    const bool qok = wait_bar(B.q_full(nu & 1), (nu >> 1) & 1, sh, p.err, p.wait_timeout_ns);
+    const bool qok = wait_bar(B.q_full(0), nu & 1, sh, p.err, p.wait_timeout_ns);
     ptx::tc_fence_after();
-    const uint32_t qb = qbase + (nu & 1) * C::kQBytes;
-    const uint32_t o_tmem = tmem + 256 + (nu & 1) * 128;
+    const uint32_t qb = qbase;
+    const uint32_t o_tmem = tmem + 128;
     auto issue_pv = [&](int jj) {
-      const bool ok = wait_bar(B.p_full(), (gm + jj) & 1, sh, p.err, p.wait_timeout_ns);
+      bool ok = wait_bar(B.p_full(), (gm + jj) & 1, sh, p.err, p.wait_timeout_ns);
+      // the first P.V of a unit overwrites O: the previous unit's epilogue
+      // must have read it
+      if (jj == 0 && nu > 0) ok = wait_bar(B.o_empty(), (nu - 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
       ptx::tc_fence_after();
       const int s = (g + jj) % C::kStages;
       const int nbk = min(kBpt, u.blk1 - (u.blk0 + kBpt * jj));
       if (ok && !*sh.abort_flag) {
         const uint32_t vb = sh.base + C::kOffV + s * C::kTileBytes;
-        const uint32_t pb = pbase + ((gm + jj) & 1) * C::kPBytes;
+        const uint32_t pb = pbase;
         for (int kk = 0; kk < nbk; ++kk) {
           const uint64_t ad = ptx::sdesc_sw128(pb + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = ptx::sdesc_sw128(vb + kk * C::kBlockBytes, 2048, 1024);
@@ -237,7 +243,7 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
         issued = true;
       }
       ptx::mma_commit(B.empty(s));
-      ptx::mma_commit(B.p_empty((gm + jj) & 1));
+      ptx::mma_commit(B.p_empty(0));
     };
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
@@ -491,34 +497,29 @@ __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1)
   return -1;
 }
 
-// Start copying unit k's query tile into the swizzled buffer at qb: row
-// tid & 127, this warpgroup's half of its 16-byte chunks (zeros past the unit's
-// rows).  Completion: cp_async_wait_all().  Returns the row's record (token,
-// visible end, partial slot); vis = 0 past the unit's rows.
+// Start copying unit k's query tile (row tid; zeros past its rows) into the
+// swizzled buffer at qb.  Completion: cp_async_wait_all().  Returns the row's
+// record (token, visible end, partial slot); vis = 0 past the unit's rows.
 template <int D>
 __device__ __forceinline__ GroupTok prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
   const UnitDesc u = p.units[k];
-  const int row = tid & 127, wg = tid >> 7;
-  const bool row_ok = row < u.nrows;
+  const bool row_ok = tid < u.nrows;
   const uint16_t* src = p.q;
   GroupTok gt{0, 0, -1, 0};
   if (row_ok) {
-    const int grow = u.row0 + row;
+    const int grow = u.row0 + tid;
     gt = p.gtoks[u.tok_off + grow / p.gqa];
     const int h = u.kvh * p.gqa + grow % p.gqa;
     src = p.q + ((size_t)gt.tok * p.hq + h) * D;
   }
-  constexpr int kHalf = D / 16;  // chunks per warpgroup
 #pragma unroll
-  for (int cc = 0; cc < kHalf; ++cc) {
-    const int c = wg * kHalf + cc;
-    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(row, c & 7), src + c * 8, row_ok ? 16u : 0u);
-  }
+  for (int c = 0; c < D / 8; ++c)
+    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), src + c * 8, row_ok ? 16u : 0u);
   ptx::cp_async_commit();
   return gt;
 }
 
-// Write columns [c0, c0 + n) of row `grow`'s result (normalised O, and lse
+// Write columns [c0, c0 + N) of row `grow`'s result (normalised O, and lse
 // when with_lse) to the output or to its partial slot.
 template <int D, int N>
 __device__ __forceinline__ void write_row_cols(const AttnParams& p, const UnitDesc& u, int grow,
@@ -540,30 +541,22 @@ __device__ __forceinline__ void write_row_cols(const AttnParams& p, const UnitDe
         make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
 }
 
-// The eight compute warps.  Tensor-core units: thread i < 128 and thread
-// i + 128 own TMEM lane (row) i together and split every tile's columns and
-// O's columns between them; they exchange one partial row max per tile
-// through shared memory.  CUDA-core units: see simt_unit.
+// The four compute warps: thread i owns TMEM lane / query row i.
 template <int D>
 __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared& sh,
                               const Bars<D>& B, uint32_t tmem) {
   using C = Cfg<D>;
-  constexpr int kCols = kTileTok / 2;  // tile columns per thread
-  constexpr int kOCols = D / 2;        // O columns per thread
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const int row = tid & 127, wg = tid >> 7;
-  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-  const uint32_t qbuf0 = sh.base + C::kOffQ;
-  float* xmax = reinterpret_cast<float*>(sh.ptr + C::kOffXM);  // [2 bufs][2 wg][128]
-  float* xl = reinterpret_cast<float*>(sh.ptr + C::kOffXL);    // [2 wg][128][2]
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t qbuf = sh.base + C::kOffQ;
+  const uint32_t o_tmem = tmem + lane_base + 128;
   uint32_t g = 0, gm = 0, nu = 0;
   GroupTok gt_next{0, 0, -1, 0};  // this thread's row record in the next tensor-core unit
-  // the first tensor-core unit's query tile, before anything else
   {
     const int first = next_mma_unit(p, u0, u1);
     if (first >= 0) {
-      gt_next = prefetch_q<D>(p, first, qbuf0, tid);
+      gt_next = prefetch_q<D>(p, first, qbuf, tid);
       ptx::cp_async_wait_all();
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(B.q_full(0));
@@ -598,16 +591,11 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       g += T;
       continue;
     }
-    // The next tensor-core unit's query tile streams into the other buffer
-    // while this unit runs (its previous user finished before our epilogue).
     const GroupTok gt_row = gt_next;
     const int vis = gt_row.vis;
     const int nxt = next_mma_unit(p, ui + 1, u1);
-    if (nxt >= 0) gt_next = prefetch_q<D>(p, nxt, qbuf0 + ((nu + 1) & 1) * C::kQBytes, tid);
-
-    const bool row_ok = row < u.nrows;
-    const bool wact = (warp & 3) * 32 < u.nrows;  // warps of padding rows keep the barriers only
-    const uint32_t o_tmem = tmem + lane_base + 256 + (nu & 1) * 128 + wg * kOCols;
+    const bool row_ok = tid < u.nrows;
+    const bool wact = warp * 32 < u.nrows;  // warps of padding rows keep the barriers only
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
@@ -616,49 +604,46 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       ok = ok && wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
+      // every QK^T of this unit has completed once the last S is ready: the
+      // query buffer is free, so the next unit's query tile starts streaming
+      if (j == T - 1 && nxt >= 0) gt_next = prefetch_q<D>(p, nxt, qbuf, tid);
       const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
-      // visible slots of this thread's two blocks (columns wg*32 .. wg*32+31)
-      int lim[2];
+      int lim[kBpt];
       bool partial = false;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
+        lim[bb] = 0;
         if (bb < nb) {
           const int mt = sh.meta[s * kBpt + bb];
           partial |= (mt & 31) < 16;
-          if ((bb >> 1) == wg) lim[bb & 1] = row_ok ? max(0, min(mt & 31, vis - (mt >> 5))) : 0;
-        } else if ((bb >> 1) == wg) {
-          lim[bb & 1] = 0;
+          if (row_ok) lim[bb] = max(0, min(mt & 31, vis - (mt >> 5)));
         }
       }
-      float sv[kCols];
+      float sv[kTileTok];
       if (ok && wact) {
-        float t32[32];
-        ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + wg * kCols, t32);
-        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < kCols; ++e) sv[e] = t32[e];
+        for (int c = 0; c < kTileTok / 32; ++c) {
+          float t32[32];
+          ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + c * 32, t32);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t32[e];
+        }
+        ptx::tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int e = 0; e < kCols; ++e) sv[e] = 0.f;
+        for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(B.s_free(sb));
-      // masked partial row max, eight independent chains; masked scores
-      // select -inf (a select, not a branch)
+      // masked row max, eight independent chains; masked scores select -inf
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kCols; ++c)
+      for (int c = 0; c < kTileTok; ++c)
         mx8[c & 7] = fmaxf(mx8[c & 7], (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY);
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // the other half of the row (double-buffered: a slow partner can still
-      // read this tile's value while we write the next tile's)
-      float* xm = xmax + ((gm + j) & 1) * 256;
-      xm[wg * 128 + row] = mx;
-      ptx::named_bar_sync(2, kComputeThreads);
-      mx = fmaxf(mx, xm[(wg ^ 1) * 128 + row]) * p.scale_log2;
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
       float m_new = m_run, alpha = 1.f;
       if (wact && mx > m_run + kRescaleLog2) {
         m_new = mx;
@@ -666,11 +651,11 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       }
       // P rounds to bf16 for the tensor cores; O is normalised by the sum of
       // the rounded weights (the weights the MMA used), lse by the exact sum.
-      uint32_t pk[kCols / 2];
+      uint32_t pk[kTileTok / 2];
       float ps4[4] = {0.f, 0.f, 0.f, 0.f}, pe4[4] = {0.f, 0.f, 0.f, 0.f};
       if (wact) {
 #pragma unroll
-        for (int c = 0; c < kCols; c += 2) {
+        for (int c = 0; c < kTileTok; c += 2) {
           const float xa = (c & 15) < lim[c >> 4] ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY;
           const float xb =
               ((c + 1) & 15) < lim[(c + 1) >> 4] ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY;
@@ -684,18 +669,13 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       l_run = fmaf(l_run, alpha, (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
       l_exact = fmaf(l_exact, alpha, (pe4[0] + pe4[1]) + (pe4[2] + pe4[3]));
       m_run = m_new;
-      // P buffer n & 1 is free once P.V of tile n - 2 has completed; O may
-      // be rescaled only after P.V of tile n - 1
-      const uint32_t n = gm + j;
-      ok = wait_bar(B.p_empty(n & 1), ((n >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
+      // the P buffer and O are free once the previous P.V has completed
+      ok = wait_bar(B.p_empty(0), (gm + j + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
       ok = __all_sync(0xffffffffu, ok);
-      const bool resc = ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-      if (resc) ok = __all_sync(0xffffffffu, wait_bar(B.p_empty((n - 1) & 1), ((n - 1) >> 1) & 1, sh,
-                                                        p.err, p.wait_timeout_ns));
       ptx::tc_fence_after();
-      if (resc && ok) {
+      if (ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int c = 0; c < kOCols / 32; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           float t32[32];
           ptx::tmem_ld32(o_tmem + c * 32, t32);
           ptx::tmem_wait_ld();
@@ -706,10 +686,10 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         ptx::tmem_wait_st();
       }
       if (wact) {
-        const uint32_t pb = sh.base + C::kOffP + (n & 1) * C::kPBytes;
+        const uint32_t pb = sh.base + C::kOffP;
 #pragma unroll
-        for (int c = 0; c < kCols / 8; ++c)
-          ptx::st_shared_v4(pb + sw128(row, wg * (kCols / 8) + c), pk[4 * c], pk[4 * c + 1],
+        for (int c = 0; c < kTileTok / 8; ++c)
+          ptx::st_shared_v4(pb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), pk[4 * c], pk[4 * c + 1],
                             pk[4 * c + 2], pk[4 * c + 3]);
       }
       if (partial) {
@@ -721,47 +701,38 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
           const int nvalid = sh.meta[s * kBpt + (r >> 4)] & 31;
           if ((r & 15) >= nvalid)
             *reinterpret_cast<uint4*>(vst + (r >> 4) * C::kBlockBytes + hh * 2048 + (r & 15) * 128 +
-                                      ch * 16) =
-                make_uint4(0, 0, 0, 0);
+                                      ch * 16) = make_uint4(0, 0, 0, 0);
         }
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(B.p_full());
     }
-    // the next unit's query tile is complete: hand it to the MMA issuer now,
-    // so its first QK^T overlaps this unit's epilogue
+    // hand the next unit's query tile to the MMA issuer, so its first QK^T
+    // overlaps this unit's epilogue
     if (nxt >= 0) {
       ptx::cp_async_wait_all();
       ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(B.q_full((nu + 1) & 1));
+      ptx::mbar_arrive(B.q_full(0));
     }
-    // ---- epilogue: O / l, row sums combined across the two halves
-    xl[(wg * 128 + row) * 2 + 0] = l_run;
-    xl[(wg * 128 + row) * 2 + 1] = l_exact;
-    ptx::named_bar_sync(2, kComputeThreads);
-    l_run += xl[((wg ^ 1) * 128 + row) * 2 + 0];
-    l_exact += xl[((wg ^ 1) * 128 + row) * 2 + 1];
+    // ---- epilogue: O / l, 32 columns at a time; then O is free again
     bool ok = wait_bar(B.o_full(), nu & 1, sh, p.err, p.wait_timeout_ns);
     ok = __all_sync(0xffffffffu, ok);
     ptx::tc_fence_after();
     if (ok && wact) {
-      float o[kOCols];
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float lse2 = l_exact > 0.f ? m_run + __log2f(l_exact) : -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kOCols / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         float t32[32];
         ptx::tmem_ld32(o_tmem + c * 32, t32);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[c * 32 + e] = t32[e];
-      }
-      ptx::tmem_wait_ld();
-      if (row_ok && !*sh.abort_flag) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const float lse2 = l_exact > 0.f ? m_run + __log2f(l_exact) : -INFINITY;
-        write_row_cols<D, kOCols>(p, u, u.row0 + row, gt_row, o, wg * kOCols, inv, lse2, wg == 0);
+        ptx::tmem_wait_ld();
+        if (row_ok && !*sh.abort_flag)
+          write_row_cols<D, 32>(p, u, u.row0 + tid, gt_row, t32, c * 32, inv, lse2, c == 0);
       }
     }
     ptx::tc_fence_before();
+    ptx::mbar_arrive(B.o_empty());
     g += T;
     gm += T;
     ++nu;
@@ -769,17 +740,17 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     tree_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
   using C = Cfg<D>;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   Shared sh;
-  {
-    const uint32_t raw = ptx::smem_u32(smem_raw);
-    const uint32_t pad = (1024 - (raw & 1023)) & 1023;
-    sh.base = raw + pad;
-    sh.ptr = smem_raw + pad;
+  sh.base = ptx::smem_u32(smem_raw);
+  sh.ptr = smem_raw;
+  if (sh.base & 1023) {  // the swizzled layouts need a 1024-byte aligned window
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, TA_DEVERR_BOUNDS);
+    return;
   }
   Bars<D> B{sh.base + C::kOffBar};
   sh.tmem_slot = reinterpret_cast<volatile uint32_t*>(sh.ptr + C::kOffBar + C::kNumBars * 8);
@@ -805,6 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(B.o_full(), 1);
     ptx::mbar_init(B.drain(), 1);
     ptx::mbar_init(B.never(), 1);  // nothing arrives here
+    ptx::mbar_init(B.o_empty(), kComputeThreads);
     *sh.abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -838,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) producer<D>(&tmk, &tmv, p, u0, u1, sh, B);
     } else if (warp == kMmaWarp) {
       if (lane == 0) mma_issuer<D>(p, u0, u1, sh, B, tmem);
-    }  // warps 10 and 11 only complete the warpgroup
+    }  // warps 6 and 7 only complete the warpgroup
     __syncwarp();
   }
   ptx::tc_fence_before();
