@@ -172,7 +172,7 @@ def bench_ours(args, rank, world, local):
     work = algorithmic_work(spec)
     q, k, v = W.make_tensors(spec, device=dev)
     torch.cuda.synchronize()
-    plan = ta.Plan.from_spec(spec)
+    plan = ta.Plan.from_spec(spec, **args.plan_opts)
     stats = plan.stats()
     out = torch.empty((spec.n_queries, spec.n_q_heads, spec.head_dim), dtype=torch.float32,
                       device=dev)
@@ -275,7 +275,8 @@ def bench_ours(args, rank, world, local):
                    "l2": "flushed before every step (512 MiB memset outside the step events)",
                    "alg_bytes_per_step": work["bytes"], "alg_flops_per_step": work["flops"],
                    "plan": {k: stats[k] for k in ("n_groups", "n_groups_mma", "n_units", "grid",
-                                                  "n_partials", "chunk_tokens", "plan_ms")}},
+                                                  "n_partials", "chunk_tokens", "plan_ms")},
+                   "plan_options": args.plan_opts},
         "e2e": {"value": round(work["bytes"] * world / (t_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -369,7 +370,13 @@ def main():
     ap.add_argument("--workload", default="long", choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--plan", action="append", default=[], metavar="KEY=VALUE",
+                    help="planner option (tree_attn_options field), e.g. --plan gamma=16")
     args = ap.parse_args()
+    args.plan_opts = {}
+    for kv in args.plan:
+        k, _, v = kv.partition("=")
+        args.plan_opts[k] = int(v)
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_env()
     if args.impl == "reference":
