@@ -96,6 +96,12 @@ typedef struct {
                                on a barrier that nothing signals, so the
                                kernel must take its timeout path (records
                                TA_DEVERR_TIMEOUT, results undefined)        */
+  int32_t merge_mode;       /* [0] 0: a separate merge kernel folds partial
+                               results after the partial-attention kernel;
+                               1: the unit that writes a row's last partial
+                               folds them (no second launch; measured slower
+                               on GB300: per-row release fences sit on the
+                               compute warps' path)                          */
 } tree_attn_options;
 
 /* Sizes of a plan, for logging and roofline accounting. */

@@ -113,3 +113,31 @@ def test_large_scores_do_not_overflow():
     out, lse, _ = run_gpu(spec, q, k, v)
     ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
     compare(out, lse, ref, ref_lse)
+
+
+# ----------------------------------------------------------------- merge modes
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_fused_and_separate_merge(merge_mode):
+    # many partials per row: a long split root and a chain of joined nodes
+    spec = W.random_tree(91, n_nodes=20, max_len=500, hq=16, hkv=4, d=128,
+                         max_queries_per_node=3)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, stats = run_gpu(spec, q, k, v, split_tokens=64, merge_mode=merge_mode)
+    assert stats["n_merge_tokens"] > 0
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    compare(out, lse, ref, ref_lse)
+
+
+def test_fused_merge_counters_reset_between_runs():
+    import tree_structured_decode_gb300 as ta
+    spec = W.config_long()
+    q, k, v = make_inputs(spec)
+    with ta.Plan.from_spec(spec) as p:
+        outs = [p.run(q, k, v) for _ in range(3)]
+        torch.cuda.synchronize()
+        assert p.device_status() == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    toks = [0, 5, 9]
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
+    compare(outs[-1][0], outs[-1][1], ref, ref_lse, toks)

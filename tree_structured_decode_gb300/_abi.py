@@ -47,6 +47,7 @@ class Options(ctypes.Structure):
         ("wait_timeout_us", ctypes.c_int32),
         ("force_edges", ctypes.POINTER(ctypes.c_int8)),
         ("debug_stuck_wait", ctypes.c_int32),
+        ("merge_mode", ctypes.c_int32),
     ]
 
 

@@ -8,11 +8,11 @@
 
 namespace ta {
 
-// Per group-token record: token id, visible end inside the group span, and
-// the partial-result index of chunk 0 (-1: the token's only partial, written
-// straight to the output).
+// Per group-token record: token id, visible end inside the group span, the
+// partial-result index of chunk 0 (-1: the token's only partial, written
+// straight to the output) and the token's number of partials.
 struct GroupTok {
-  int32_t tok, vis, pbase, pad;
+  int32_t tok, vis, pbase, pcount;
 };
 
 // Per merge item: a query token with >= 2 partials.
@@ -37,6 +37,12 @@ struct AttnParams {
   float scale_log2;          // softmax scale * log2(e)
   long long wait_timeout_ns;
   int32_t debug_stuck_wait;  // testing aid: wait on a barrier nothing signals
+  // fused merge: per (token, q head) arrival counters (zero between runs)
+  // and each token's first partial index; merge_fused = 0 leaves the
+  // partials to the separate merge kernel
+  int32_t* merge_cnt;
+  const int32_t* tok_poff;
+  int32_t merge_fused;
 };
 
 struct MergeParams {

@@ -25,6 +25,9 @@ struct tree_attn_plan_s {
   int32_t* d_err = nullptr;
   float* d_part_o = nullptr;
   float* d_part_lse = nullptr;
+  int32_t* d_merge_cnt = nullptr;
+  size_t merge_cnt_bytes = 0;
+  const int32_t* d_tok_poff = nullptr;
   double plan_ms = 0.0;
   bool profiling = false;
   bool profiled_run = false;

@@ -41,6 +41,7 @@ struct Options {
   int32_t wait_timeout_us = 2000000;
   std::vector<int8_t> force_edges;  // empty = greedy
   int32_t debug_stuck_wait = 0;
+  int32_t merge_mode = 0;  // 0 separate merge kernel, 1 fused into the partial kernel
 };
 
 // One work unit as the kernels read it (32 bytes, device POD).

@@ -45,6 +45,7 @@ ta::Options to_options(const tree_attn_options* o) {
   r.host_only = o->host_only;
   if (o->wait_timeout_us) r.wait_timeout_us = o->wait_timeout_us;
   r.debug_stuck_wait = o->debug_stuck_wait;
+  r.merge_mode = o->merge_mode;
   return r;
 }
 
@@ -54,7 +55,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 tree_attn_status upload(tree_attn_plan_s* P) {
   const ta::HostPlan& h = P->hp;
   std::vector<ta::GroupTok> gt(h.gtok.size());
-  for (size_t i = 0; i < gt.size(); ++i) gt[i] = {h.gtok[i], h.gvis[i], h.gpbase[i], 0};
+  for (size_t i = 0; i < gt.size(); ++i)
+    gt[i] = {h.gtok[i], h.gvis[i], h.gpbase[i], h.pcount[h.gtok[i]]};
   std::vector<int2> blocks(h.blk_page.size());
   for (size_t i = 0; i < blocks.size(); ++i) blocks[i] = make_int2(h.blk_page[i], h.blk_meta[i]);
   std::vector<ta::MergeItem> merge(h.merge_tok.size());
@@ -67,13 +69,14 @@ tree_attn_status upload(tree_attn_plan_s* P) {
     size_t bytes;
     size_t off;
   };
-  Sec secs[6] = {
+  Sec secs[7] = {
       {h.units.data(), h.units.size() * sizeof(ta::UnitDesc), 0},
       {blocks.data(), blocks.size() * sizeof(int2), 0},
       {gt.data(), gt.size() * sizeof(ta::GroupTok), 0},
       {h.cta_off.data(), h.cta_off.size() * sizeof(int32_t), 0},
       {merge.data(), merge.size() * sizeof(ta::MergeItem), 0},
       {nullptr, 16 * sizeof(int32_t), 0},  // error word(s)
+      {h.poff.data(), h.poff.size() * sizeof(int32_t), 0},
   };
   size_t off = 0;
   for (auto& s : secs) {
@@ -98,11 +101,13 @@ tree_attn_status upload(tree_attn_plan_s* P) {
   P->d_cta_off = reinterpret_cast<const int32_t*>(b + secs[3].off);
   P->d_merge = reinterpret_cast<const ta::MergeItem*>(b + secs[4].off);
   P->d_err = reinterpret_cast<int32_t*>(b + secs[5].off);
+  P->d_tok_poff = reinterpret_cast<const int32_t*>(b + secs[6].off);
 
   const size_t np = (size_t)h.n_partials * h.hq;
   const size_t o_bytes = align_up(np * h.d * sizeof(float), 256);
   const size_t l_bytes = align_up(np * sizeof(float), 256);
-  P->work_bytes = o_bytes + l_bytes;
+  const size_t c_bytes = h.n_partials ? align_up((size_t)h.nq * h.hq * sizeof(int32_t), 256) : 0;
+  P->work_bytes = o_bytes + l_bytes + c_bytes;
   if (P->work_bytes) {
     e = cudaMalloc(&P->dwork, P->work_bytes);
     if (e != cudaSuccess) {
@@ -111,6 +116,12 @@ tree_attn_status upload(tree_attn_plan_s* P) {
     }
     P->d_part_o = static_cast<float*>(P->dwork);
     P->d_part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(P->dwork) + o_bytes);
+    if (c_bytes) {
+      P->d_merge_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(P->dwork) + o_bytes + l_bytes);
+      P->merge_cnt_bytes = c_bytes;
+      e = cudaMemset(P->d_merge_cnt, 0, c_bytes);
+      if (e != cudaSuccess) return cuda_err(e, "cudaMemset(merge counters)");
+    }
   }
   return TA_OK;
 }
@@ -246,15 +257,18 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
   ap.scale_log2 = h.scale * 1.4426950408889634f;
   ap.wait_timeout_ns = (long long)h.opt.wait_timeout_us * 1000ll;
   ap.debug_stuck_wait = h.opt.debug_stuck_wait;
+  ap.merge_cnt = P->d_merge_cnt;
+  ap.tok_poff = P->d_tok_poff;
+  static const bool simple = [] {
+    const char* v = std::getenv("TREE_ATTN_SIMPLE_KERNEL");
+    return v && v[0] == '1';
+  }();
+  ap.merge_fused = (h.opt.merge_mode == 1 && !simple) ? 1 : 0;
   cudaError_t e;
   if (P->profiling) {
     e = cudaEventRecord(P->ev[0], s);
     if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord");
   }
-  static const bool simple = [] {
-    const char* v = std::getenv("TREE_ATTN_SIMPLE_KERNEL");
-    return v && v[0] == '1';
-  }();
   e = simple ? ta::launch_partial_attention(ap, h.d, h.grid, s)
              : ta::launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
   if (e != cudaSuccess) return cuda_err(e, "partial attention launch");
@@ -262,7 +276,7 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
     e = cudaEventRecord(P->ev[1], s);
     if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord");
   }
-  if (!h.merge_tok.empty()) {
+  if (!h.merge_tok.empty() && !ap.merge_fused) {
     ta::MergeParams mp{};
     mp.items = P->d_merge;
     mp.n_items = (int32_t)h.merge_tok.size();
@@ -280,7 +294,7 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
   }
   if (P->profiling) {
     P->profiled_run = true;
-    P->profiled_merge = !h.merge_tok.empty();
+    P->profiled_merge = !h.merge_tok.empty() && !ap.merge_fused;
   }
   return TA_OK;
 }
@@ -337,6 +351,11 @@ tree_attn_status tree_attn_device_status(tree_attn_plan_t P, void* stream, int32
   e = cudaMemset(P->d_err, 0, sizeof w);
   if (e != cudaSuccess) return cuda_err(e, "clear device status");
   *code = w[0];
+  if (w[0] != TA_DEVERR_NONE && P->d_merge_cnt) {
+    // an aborted run can leave merge counters part-way: start them afresh
+    e = cudaMemset(P->d_merge_cnt, 0, P->merge_cnt_bytes);
+    if (e != cudaSuccess) return cuda_err(e, "clear merge counters");
+  }
   if (w[0] != TA_DEVERR_NONE)
     return set_err(TA_ERR_DEVICE, "kernel reported device error " + std::to_string(w[0]) +
                                       " (detail " + std::to_string(w[1]) + ")");

@@ -55,11 +55,12 @@ __global__ void pack_tables(const int32_t* blk_page, const int32_t* blk_meta, in
                             int2* blocks, const int32_t* gtok, const int32_t* gvis,
                             const int32_t* gpbase, int ntok, GroupTok* gtoks,
                             const int32_t* merge_tok, const int32_t* poff, const int32_t* pcount,
-                            int nmerge, MergeItem* merge, int32_t* err) {
-  const int n = max(nblk, max(ntok, nmerge));
+                            int nmerge, MergeItem* merge, int32_t* err, int32_t* cnt, int ncnt) {
+  const int n = max(max(nblk, ntok), max(nmerge, ncnt));
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     if (i < nblk) blocks[i] = make_int2(blk_page[i], blk_meta[i]);
-    if (i < ntok) gtoks[i] = GroupTok{gtok[i], gvis[i], gpbase[i], 0};
+    if (i < ntok) gtoks[i] = GroupTok{gtok[i], gvis[i], gpbase[i], pcount[gtok[i]]};
+    if (i < ncnt) cnt[i] = 0;  // fused-merge arrival counters start at zero
     if (i < nmerge) {
       const int t = merge_tok[i];
       merge[i] = MergeItem{t, poff[t], pcount[t], 0};
@@ -112,6 +113,8 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   const size_t o_err = take(16 * sizeof(int32_t));
   const size_t o_po = take(np * (size_t)h.d * sizeof(float));
   const size_t o_pl = take(np * sizeof(float));
+  const size_t ncnt = h.n_partials ? nq * (size_t)h.hq : 0;
+  const size_t o_cnt = take(ncnt * sizeof(int32_t));
   if (off > kScratchBytes)
     return fail(TA_ERR_UNSUPPORTED,
                 "this plan needs " + std::to_string(off) + " bytes of scratch; the static scratch "
@@ -151,7 +154,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
     e = cudaMemcpyAsync(base + c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
   }
-  const size_t nmax = std::max(nblk, std::max(ntok, nmerge));
+  const size_t nmax = std::max(std::max(nblk, ntok), std::max(nmerge, ncnt));
   const int pack_blocks = (int)std::min<size_t>(std::max<size_t>((nmax + 255) / 256, 1), 1024);
   pack_tables<<<pack_blocks, 256, 0, s>>>(
       reinterpret_cast<const int32_t*>(base + o_bpage), reinterpret_cast<const int32_t*>(base + o_bmeta),
@@ -161,7 +164,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
       reinterpret_cast<GroupTok*>(base + o_gtoks), reinterpret_cast<const int32_t*>(base + o_mtok),
       reinterpret_cast<const int32_t*>(base + o_poff), reinterpret_cast<const int32_t*>(base + o_pcnt),
       (int)nmerge, reinterpret_cast<MergeItem*>(base + o_merge),
-      reinterpret_cast<int32_t*>(base + o_err));
+      reinterpret_cast<int32_t*>(base + o_err), reinterpret_cast<int32_t*>(base + o_cnt), (int)ncnt);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("table pack launch: ") + cudaGetErrorString(e));
 
@@ -186,9 +189,12 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   ap.scale_log2 = h.scale * 1.4426950408889634f;
   ap.wait_timeout_ns = (long long)h.opt.wait_timeout_us * 1000ll;
   ap.debug_stuck_wait = h.opt.debug_stuck_wait;
+  ap.merge_cnt = reinterpret_cast<int32_t*>(base + o_cnt);
+  ap.tok_poff = reinterpret_cast<const int32_t*>(base + o_poff);
+  ap.merge_fused = h.opt.merge_mode == 1 ? 1 : 0;
   e = launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
   if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("partial attention launch: ") + cudaGetErrorString(e));
-  if (nmerge) {
+  if (nmerge && !ap.merge_fused) {
     MergeParams mp{};
     mp.items = reinterpret_cast<const MergeItem*>(base + o_merge);
     mp.n_items = (int32_t)nmerge;

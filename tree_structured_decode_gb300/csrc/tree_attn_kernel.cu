@@ -284,6 +284,99 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
+// ---------------------------------------------------------- fused merge
+// After a row's partial (O normalised, lse in base 2) is written, its writer
+// counts it in; the writer of the row's last partial folds all of them:
+//   m = max lse_i, w_i = 2^(lse_i - m), O = sum w_i O_i / sum w_i,
+//   lse = m + log2 sum w_i
+// (DeFT notes page, "Tree-Topology-Aware Global Reduction Strategy"), writes
+// the output row and resets the counter for the next run.  Release: a fence
+// before the count; acquire: a fence after observing the last count; the
+// partials are read through L2 (other SMs wrote them).
+
+// One thread folds row (tok, h).  Returns nothing; no-op unless last.
+template <int D>
+__device__ void merge_row_thread(const AttnParams& p, const GroupTok& gt, int h) {
+  const int idx = gt.tok * p.hq + h;
+  __threadfence();
+  if (atomicAdd(p.merge_cnt + idx, 1) != gt.pcount - 1) return;
+  __threadfence();
+  const int poff = __ldcg(p.tok_poff + gt.tok);
+  float m = -INFINITY;
+  for (int k = 0; k < gt.pcount; ++k) m = fmaxf(m, __ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h));
+  float* dst = p.out + (size_t)idx * D;
+  float den = 0.f;
+  if (m == -INFINITY) {
+    for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    for (int k = 0; k < gt.pcount; ++k)
+      den += ptx::ex2(__ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h) - m);
+    const float inv = 1.f / den;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      float4 acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < gt.pcount; ++k) {
+        const size_t slot = (size_t)(poff + k) * p.hq + h;
+        const float w = ptx::ex2(__ldcg(p.part_lse + slot) - m);
+        const float4* src = reinterpret_cast<const float4*>(p.part_o + slot * D + c0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 v = __ldcg(src + e);
+          acc[e].x = fmaf(w, v.x, acc[e].x);
+          acc[e].y = fmaf(w, v.y, acc[e].y);
+          acc[e].z = fmaf(w, v.z, acc[e].z);
+          acc[e].w = fmaf(w, v.w, acc[e].w);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        *reinterpret_cast<float4*>(dst + c0 + 4 * e) =
+            make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv);
+    }
+  }
+  if (p.lse) p.lse[idx] = m == -INFINITY ? -INFINITY : (m + __log2f(den)) * kLn2;
+  p.merge_cnt[idx] = 0;
+}
+
+// A warp folds row (tok, h), lanes over d (lane holds EPL columns).
+template <int D>
+__device__ void merge_row_warp(const AttnParams& p, const GroupTok& gt, int h, int lane) {
+  constexpr int EPL = D / 32;
+  const int idx = gt.tok * p.hq + h;
+  int last = 0;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    last = atomicAdd(p.merge_cnt + idx, 1) == gt.pcount - 1;
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  const int poff = __ldcg(p.tok_poff + gt.tok);
+  float m = -INFINITY;
+  for (int k = 0; k < gt.pcount; ++k) m = fmaxf(m, __ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h));
+  float acc[EPL], den = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  if (m != -INFINITY) {
+    for (int k = 0; k < gt.pcount; ++k) {
+      const size_t slot = (size_t)(poff + k) * p.hq + h;
+      const float w = ptx::ex2(__ldcg(p.part_lse + slot) - m);
+      den += w;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, __ldcg(p.part_o + slot * D + lane * EPL + e), acc[e]);
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) p.out[(size_t)idx * D + lane * EPL + e] = acc[e] * inv;
+  if (lane == 0) {
+    if (p.lse) p.lse[idx] = den > 0.f ? (m + __log2f(den)) * kLn2 : -INFINITY;
+    p.merge_cnt[idx] = 0;
+  }
+}
+
 template <int EPL>
 __device__ __forceinline__ void load_slice(const uint8_t* ptr, float (&f)[EPL]) {
   if constexpr (EPL == 4) {
@@ -466,7 +559,7 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
         for (int e = 0; e < EPL; ++e) O[e] = fmaf(sm_o[(w * RB + i) * D + lane * EPL + e], sc, O[e]);
       }
     }
-    if (!*sh.abort_flag) {
+    if (__shfl_sync(0xffffffffu, *sh.abort_flag == 0, 0)) {  // warp-uniform
       const int grow = u.row0 + i;
       const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
       const int h = u.kvh * p.gqa + grow % p.gqa;
@@ -483,6 +576,7 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
       }
 #pragma unroll
       for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = O[e] * inv;
+      if (gt.pbase >= 0 && p.merge_fused) merge_row_warp<D>(p, gt, h, lane);
     }
   }
   ptx::named_bar_sync(1, kComputeThreads);
@@ -583,6 +677,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         }
         for (int c = 0; c < D; c += 4)
           *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (gt.pbase >= 0 && p.merge_fused) merge_row_thread<D>(p, gt, h);
       }
       continue;
     }
@@ -732,7 +827,9 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       }
     }
     ptx::tc_fence_before();
-    ptx::mbar_arrive(B.o_empty());
+    ptx::mbar_arrive(B.o_empty());  // O is free before the (rare, slow) merge
+    if (ok && row_ok && gt_row.pbase >= 0 && p.merge_fused && !*sh.abort_flag)
+      merge_row_thread<D>(p, gt_row, u.kvh * p.gqa + (u.row0 + tid) % p.gqa);
     g += T;
     gm += T;
     ++nu;
