@@ -102,6 +102,9 @@ typedef struct {
                                folds them (no second launch; measured slower
                                on GB300: per-row release fences sit on the
                                compute warps' path)                          */
+  int32_t no_pack;          /* [0] 1: never pack thin groups (up to four
+                               short groups of one kv head sharing a unit,
+                               one page of each per KV tile)                 */
 } tree_attn_options;
 
 /* Sizes of a plan, for logging and roofline accounting. */

@@ -48,6 +48,7 @@ class PlannerOptions:
     split_waves: int = 4                 # automatic split aims at waves x SMs
     num_sms: int = 152                   # SM count the split targets
     force_path: int = 0                  # 0 by rows, 1 CUDA cores, 2 MMA
+    no_pack: int = 0                     # 1: never pack thin groups
     edges: tuple | None = field(default=None)  # force an assignment (tests)
 
 
@@ -263,7 +264,23 @@ def build_plan(parent, node_kv_len, node_page_offsets, node_pages, page_size,
     for g in groups:
         for t in g["tokens"]:
             count[t] += len(g["chunks"])
-    n_units = sum(n_kv_heads * g["qtiles"] * len(g["chunks"]) for g in groups)
+    # Thin-group packing: up to 4 short single-chunk tensor-core groups of one
+    # kv head share a unit (one page of each per KV tile); at most 32 rows per
+    # slot, and the GQA ratio must divide 32.
+    def packable(g):
+        if o.no_pack or len(g["chunks"]) != 1 or g["qtiles"] != 1:
+            return None
+        nb = len(g["blocks"])
+        if nb < 1 or nb > 8:
+            return None
+        if g["path"] == "mma" and g["rows"] <= 32 and 32 % r == 0:
+            return "mma"
+        return None  # CUDA-core groups are not packed
+    kinds = [packable(g) for g in groups]
+    n_units = sum(n_kv_heads * g["qtiles"] * len(g["chunks"])
+                  for g, k in zip(groups, kinds) if k is None)
+    for kind in ("mma", "simt"):
+        n_units += n_kv_heads * _ceil(sum(1 for k in kinds if k == kind), 4)
     return {
         "edges": edge,
         "chunk_blocks": chunk,

@@ -141,3 +141,22 @@ def test_fused_merge_counters_reset_between_runs():
     toks = [0, 5, 9]
     ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
     compare(outs[-1][0], outs[-1][1], ref, ref_lse, toks)
+
+
+# ----------------------------------------------------------------- packed thin groups
+@pytest.mark.parametrize("hq,hkv,path", [(4, 4, 2), (8, 4, 2), (16, 4, 2), (32, 4, 2), (8, 8, 1)])
+def test_packed_thin_groups(hq, hkv, path):
+    # many short leaves (<= 8 pages) under one root: leaves pack four to a
+    # unit; force_path picks CUDA-core packs (<= 2 rows) or tensor-core packs
+    spec = W.two_level(300, 23, 0, hq, hkv, 128, seed=hq + path)
+    rng = np.random.default_rng(hq)
+    lens = [300] + [int(x) for x in rng.integers(1, 129, size=23)]
+    spec = W._finish("packs", spec.parent, lens,
+                     [v for v in range(1, 24) for _ in range(1 + v % 2)],
+                     [lens[v] - j for v in range(1, 24) for j in range(1 + v % 2)],
+                     hq, hkv, 128, seed=5)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    for opts in ({"force_path": path}, {"force_path": path, "no_pack": 1}):
+        out, lse, _ = run_gpu(spec, q, k, v, **opts)
+        ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+        compare(out, lse, ref, ref_lse)

@@ -23,7 +23,7 @@ def _native(spec, **opt):
 def _reference(spec, **opt):
     o = P.PlannerOptions(num_sms=opt.get("num_sms", 152))
     for k in ("gamma", "beta", "ts_c", "mma_min_rows", "split_tokens", "min_split_tokens",
-              "split_waves", "force_path"):
+              "split_waves", "force_path", "no_pack"):
         if k in opt:
             setattr(o, k, opt[k])
     if "ts_q_set" in opt:
@@ -90,6 +90,15 @@ def test_forced_edge_assignments_match_reference(seed):
     edges = rng.integers(0, 2, size=spec.n_nodes).astype(np.int8)
     edges[0] = 0
     _same(spec, force_edges=edges, split_tokens=int(rng.choice([0, 32, 64])))
+
+
+@pytest.mark.parametrize("name", ["wide"])
+def test_packing_can_be_disabled(name):
+    spec = W.CONFIGS[name]()
+    packed, _ = _same(spec)
+    plain, _ = _same(spec, no_pack=1)
+    assert packed["units"] < plain["units"]
+    assert packed["groups"] == plain["groups"]
 
 
 def test_planning_is_fast_on_the_irregular_tree():

@@ -48,6 +48,7 @@ class Options(ctypes.Structure):
         ("force_edges", ctypes.POINTER(ctypes.c_int8)),
         ("debug_stuck_wait", ctypes.c_int32),
         ("merge_mode", ctypes.c_int32),
+        ("no_pack", ctypes.c_int32),
     ]
 
 

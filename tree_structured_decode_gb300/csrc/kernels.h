@@ -8,12 +8,19 @@
 
 namespace ta {
 
-// Per group-token record: token id, visible end inside the group span, the
-// partial-result index of chunk 0 (-1: the token's only partial, written
-// straight to the output) and the token's number of partials.
+// Per group-token record (16 bytes): token id (-1: a filler row of a packed
+// unit), visible end inside the group span, the partial-result index of
+// chunk 0 (-1: the token's only partial, written straight to the output),
+// and pc_slot = the token's number of partials (low 24 bits) | (the page
+// slot a packed row sees + 1) << 24 (0: every page of the tile).
 struct GroupTok {
-  int32_t tok, vis, pbase, pcount;
+  int32_t tok, vis, pbase, pc_slot;
+  __host__ __device__ int pcount() const { return pc_slot & 0xFFFFFF; }
+  __host__ __device__ int slot() const { return (pc_slot >> 24) - 1; }
 };
+__host__ __device__ inline int32_t pack_pc_slot(int32_t pcount, int32_t slot) {
+  return (pcount & 0xFFFFFF) | ((slot + 1) << 24);
+}
 
 // Per merge item: a query token with >= 2 partials.
 struct MergeItem {
@@ -54,8 +61,6 @@ struct MergeParams {
   float* lse;
 };
 
-// Launch the partial-attention pass (every unit).  Returns the launch error.
-cudaError_t launch_partial_attention(const AttnParams& p, int d, int grid, cudaStream_t s);
 // Launch the persistent grouped partial-attention kernel (TMA + tcgen05 /
 // CUDA cores), one CTA per schedule entry.
 cudaError_t launch_tree_attention(const AttnParams& p, int d, int grid, int num_pages,

@@ -344,7 +344,23 @@ tree_attn_status build_host_plan(
   }
 
   // ------------------------------------------ units and LPT schedule
+  p.gslot.assign(p.gtok.size(), -1);
+  auto packable = [&](const GroupInfo& g) {
+    if (opt.no_pack || g.nchunks != 1 || g.qtiles != 1 || g.nblk < 1 || g.nblk > kPackMaxBlocks)
+      return -1;
+    if (g.path == kPathMma && g.rows <= kPackMmaRows && kPackMmaRows % r == 0) return (int)kPathMma;
+    // CUDA-core groups are not packed: measured slower (fewer, longer units
+    // balance worse than the per-unit overhead they save)
+    return -1;
+  };
+  std::vector<int32_t> pack_mma, pack_simt;  // group indices, in group order
+  for (size_t gi = 0; gi < p.groups.size(); ++gi) {
+    const int k = packable(p.groups[gi]);
+    if (k == kPathMma) pack_mma.push_back((int32_t)gi);
+    if (k == kPathSimt) pack_simt.push_back((int32_t)gi);
+  }
   for (auto& g : p.groups) {
+    if (packable(g) >= 0) continue;
     const int tile = g.path == kPathMma ? kMmaTileRows : kSimtTileRows;
     for (int kvh = 0; kvh < hkv; ++kvh)
       for (int c = 0; c < g.nchunks; ++c)
@@ -361,6 +377,63 @@ tree_attn_status build_host_plan(
           p.units.push_back(u);
         }
   }
+  // Packed units: row records laid out slot by slot (slot_rows rows per
+  // slot; filler records have tok -1), and an interleaved block list
+  // (tile j = page j of each slot's group, zero-valid filler pages past a
+  // group's end or for an empty slot).  Records and blocks do not depend on
+  // the kv head, so all kv heads share them.
+  auto emit_packs = [&](const std::vector<int32_t>& list, int path) {
+    const int slot_rows = path == kPathMma ? kPackMmaRows : kPackSimtRows;
+    for (size_t s0 = 0; s0 < list.size(); s0 += kPackSlots) {
+      const size_t ns = std::min<size_t>(kPackSlots, list.size() - s0);
+      const int32_t tok_off = (int32_t)p.gtok.size();
+      for (int k = 0; k < kPackSlots; ++k) {
+        const GroupInfo* g = (size_t)k < ns ? &p.groups[list[s0 + k]] : nullptr;
+        for (int e = 0; e < slot_rows / r; ++e) {
+          if (g && e < g->ntok) {
+            p.gtok.push_back(p.gtok[g->tok_off + e]);
+            p.gvis.push_back(p.gvis[g->tok_off + e]);
+            p.gpbase.push_back(p.gpbase[g->tok_off + e]);
+          } else {
+            p.gtok.push_back(-1);
+            p.gvis.push_back(0);
+            p.gpbase.push_back(-1);
+          }
+          p.gslot.push_back(k);
+        }
+      }
+      int tiles = 0;
+      for (size_t k = 0; k < ns; ++k) tiles = std::max(tiles, p.groups[list[s0 + k]].nblk);
+      const int32_t blk0 = (int32_t)p.blk_page.size();
+      const int32_t filler_page = p.blk_page[p.groups[list[s0]].blk_off];
+      for (int t = 0; t < tiles; ++t)
+        for (int k = 0; k < kPackSlots; ++k) {
+          const GroupInfo* g = (size_t)k < ns ? &p.groups[list[s0 + k]] : nullptr;
+          if (g && t < g->nblk) {
+            p.blk_page.push_back(p.blk_page[g->blk_off + t]);
+            p.blk_meta.push_back(p.blk_meta[g->blk_off + t]);
+          } else {
+            p.blk_page.push_back(filler_page);
+            p.blk_meta.push_back(0);
+          }
+        }
+      const int32_t blk1 = (int32_t)p.blk_page.size();
+      for (int kvh = 0; kvh < hkv; ++kvh) {
+        UnitDesc u;
+        u.tok_off = tok_off;
+        u.kvh = kvh;
+        u.row0 = 0;
+        u.nrows = kPackSlots * slot_rows;
+        u.blk0 = blk0;
+        u.blk1 = blk1;
+        u.chunk = 0;
+        u.path = path;
+        p.units.push_back(u);
+      }
+    }
+  };
+  emit_packs(pack_mma, kPathMma);
+  emit_packs(pack_simt, kPathSimt);
   const int64_t nu = (int64_t)p.units.size();
   p.grid = (int32_t)std::min<int64_t>(nu, (int64_t)std::max(1, opt.num_sms) * kCtasPerSm);
   {

@@ -23,6 +23,14 @@ constexpr int kBlocksPerTile = kKvTileTokens / kPageSize;
 constexpr int kMmaTileRows = 128;                  // tcgen05 M
 constexpr int kSimtTileRows = 8;                   // CUDA-core rows per unit
 constexpr int kCtasPerSm = 2;                      // co-resident persistent CTAs per SM
+// Thin-group packing: up to kPackSlots short groups of one kv head share a
+// unit; tile j carries page j of every packed group (one page per slot) and
+// each group's rows see only their slot.
+constexpr int kPackSlots = 4;
+constexpr int kPackMaxBlocks = 8;   // groups of at most 8 pages (128 tokens)
+constexpr int kPackMmaRows = 32;    // rows per slot on tensor cores (one warp)
+constexpr int kPackSimtRows = 2;    // rows per slot on CUDA cores
+static_assert(kPackSlots == kBlocksPerTile, "one page per slot per tile");
 constexpr int kPathSimt = 0;
 constexpr int kPathMma = 1;
 
@@ -42,6 +50,7 @@ struct Options {
   std::vector<int8_t> force_edges;  // empty = greedy
   int32_t debug_stuck_wait = 0;
   int32_t merge_mode = 0;  // 0 separate merge kernel, 1 fused into the partial kernel
+  int32_t no_pack = 0;     // 1: never pack thin groups
 };
 
 // One work unit as the kernels read it (32 bytes, device POD).
@@ -80,6 +89,7 @@ struct HostPlan {
   std::vector<GroupInfo> groups;
   std::vector<int32_t> chain_nodes;
   std::vector<int32_t> gtok, gvis, gpbase;
+  std::vector<int32_t> gslot;                // -1, or the page slot of a packed row (tok -1: filler row)
   std::vector<int32_t> blk_page, blk_meta;   // meta = span_pos * 32 + valid
   std::vector<int32_t> chunk_lo, chunk_hi;
   int64_t chunk_blocks = 0;

@@ -46,6 +46,7 @@ ta::Options to_options(const tree_attn_options* o) {
   if (o->wait_timeout_us) r.wait_timeout_us = o->wait_timeout_us;
   r.debug_stuck_wait = o->debug_stuck_wait;
   r.merge_mode = o->merge_mode;
+  r.no_pack = o->no_pack;
   return r;
 }
 
@@ -56,7 +57,8 @@ tree_attn_status upload(tree_attn_plan_s* P) {
   const ta::HostPlan& h = P->hp;
   std::vector<ta::GroupTok> gt(h.gtok.size());
   for (size_t i = 0; i < gt.size(); ++i)
-    gt[i] = {h.gtok[i], h.gvis[i], h.gpbase[i], h.pcount[h.gtok[i]]};
+    gt[i] = {h.gtok[i], h.gvis[i], h.gpbase[i],
+             ta::pack_pc_slot(h.gtok[i] >= 0 ? h.pcount[h.gtok[i]] : 0, h.gslot[i])};
   std::vector<int2> blocks(h.blk_page.size());
   for (size_t i = 0; i < blocks.size(); ++i) blocks[i] = make_int2(h.blk_page[i], h.blk_meta[i]);
   std::vector<ta::MergeItem> merge(h.merge_tok.size());
@@ -259,18 +261,13 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
   ap.debug_stuck_wait = h.opt.debug_stuck_wait;
   ap.merge_cnt = P->d_merge_cnt;
   ap.tok_poff = P->d_tok_poff;
-  static const bool simple = [] {
-    const char* v = std::getenv("TREE_ATTN_SIMPLE_KERNEL");
-    return v && v[0] == '1';
-  }();
-  ap.merge_fused = (h.opt.merge_mode == 1 && !simple) ? 1 : 0;
+  ap.merge_fused = h.opt.merge_mode == 1 ? 1 : 0;
   cudaError_t e;
   if (P->profiling) {
     e = cudaEventRecord(P->ev[0], s);
     if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord");
   }
-  e = simple ? ta::launch_partial_attention(ap, h.d, h.grid, s)
-             : ta::launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
+  e = ta::launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
   if (e != cudaSuccess) return cuda_err(e, "partial attention launch");
   if (P->profiling) {
     e = cudaEventRecord(P->ev[1], s);

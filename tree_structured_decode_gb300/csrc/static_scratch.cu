@@ -53,13 +53,15 @@ cudaError_t scratch_base(int dev, void** out) {
 // clear the error words.
 __global__ void pack_tables(const int32_t* blk_page, const int32_t* blk_meta, int nblk,
                             int2* blocks, const int32_t* gtok, const int32_t* gvis,
-                            const int32_t* gpbase, int ntok, GroupTok* gtoks,
+                            const int32_t* gpbase, const int32_t* gslot, int ntok, GroupTok* gtoks,
                             const int32_t* merge_tok, const int32_t* poff, const int32_t* pcount,
                             int nmerge, MergeItem* merge, int32_t* err, int32_t* cnt, int ncnt) {
   const int n = max(max(nblk, ntok), max(nmerge, ncnt));
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     if (i < nblk) blocks[i] = make_int2(blk_page[i], blk_meta[i]);
-    if (i < ntok) gtoks[i] = GroupTok{gtok[i], gvis[i], gpbase[i], pcount[gtok[i]]};
+    if (i < ntok)
+      gtoks[i] = GroupTok{gtok[i], gvis[i], gpbase[i],
+                          pack_pc_slot(gtok[i] >= 0 ? pcount[gtok[i]] : 0, gslot[i])};
     if (i < ncnt) cnt[i] = 0;  // fused-merge arrival counters start at zero
     if (i < nmerge) {
       const int t = merge_tok[i];
@@ -107,6 +109,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   const size_t o_cta = take(h.cta_off.size() * sizeof(int32_t));
   const size_t o_bpage = take(nblk * 4), o_bmeta = take(nblk * 4), o_blocks = take(nblk * 8);
   const size_t o_gtok = take(ntok * 4), o_gvis = take(ntok * 4), o_gpb = take(ntok * 4);
+  const size_t o_gslot = take(ntok * 4);
   const size_t o_gtoks = take(ntok * sizeof(GroupTok));
   const size_t o_mtok = take(nmerge * 4), o_poff = take(nq * 4), o_pcnt = take(nq * 4);
   const size_t o_merge = take(nmerge * sizeof(MergeItem));
@@ -145,6 +148,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
       {o_gtok, h.gtok.data(), ntok * 4},
       {o_gvis, h.gvis.data(), ntok * 4},
       {o_gpb, h.gpbase.data(), ntok * 4},
+      {o_gslot, h.gslot.data(), ntok * 4},
       {o_mtok, h.merge_tok.data(), nmerge * 4},
       {o_poff, h.poff.data(), nq * 4},
       {o_pcnt, h.pcount.data(), nq * 4},
@@ -160,7 +164,8 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
       reinterpret_cast<const int32_t*>(base + o_bpage), reinterpret_cast<const int32_t*>(base + o_bmeta),
       (int)nblk, reinterpret_cast<int2*>(base + o_blocks),
       reinterpret_cast<const int32_t*>(base + o_gtok), reinterpret_cast<const int32_t*>(base + o_gvis),
-      reinterpret_cast<const int32_t*>(base + o_gpb), (int)ntok,
+      reinterpret_cast<const int32_t*>(base + o_gpb), reinterpret_cast<const int32_t*>(base + o_gslot),
+      (int)ntok,
       reinterpret_cast<GroupTok*>(base + o_gtoks), reinterpret_cast<const int32_t*>(base + o_mtok),
       reinterpret_cast<const int32_t*>(base + o_poff), reinterpret_cast<const int32_t*>(base + o_pcnt),
       (int)nmerge, reinterpret_cast<MergeItem*>(base + o_merge),

@@ -299,17 +299,17 @@ template <int D>
 __device__ void merge_row_thread(const AttnParams& p, const GroupTok& gt, int h) {
   const int idx = gt.tok * p.hq + h;
   __threadfence();
-  if (atomicAdd(p.merge_cnt + idx, 1) != gt.pcount - 1) return;
+  if (atomicAdd(p.merge_cnt + idx, 1) != gt.pcount() - 1) return;
   __threadfence();
   const int poff = __ldcg(p.tok_poff + gt.tok);
   float m = -INFINITY;
-  for (int k = 0; k < gt.pcount; ++k) m = fmaxf(m, __ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h));
+  for (int k = 0; k < gt.pcount(); ++k) m = fmaxf(m, __ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h));
   float* dst = p.out + (size_t)idx * D;
   float den = 0.f;
   if (m == -INFINITY) {
     for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   } else {
-    for (int k = 0; k < gt.pcount; ++k)
+    for (int k = 0; k < gt.pcount(); ++k)
       den += ptx::ex2(__ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h) - m);
     const float inv = 1.f / den;
 #pragma unroll 1
@@ -317,7 +317,7 @@ __device__ void merge_row_thread(const AttnParams& p, const GroupTok& gt, int h)
       float4 acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = 0; k < gt.pcount; ++k) {
+      for (int k = 0; k < gt.pcount(); ++k) {
         const size_t slot = (size_t)(poff + k) * p.hq + h;
         const float w = ptx::ex2(__ldcg(p.part_lse + slot) - m);
         const float4* src = reinterpret_cast<const float4*>(p.part_o + slot * D + c0);
@@ -349,18 +349,18 @@ __device__ void merge_row_warp(const AttnParams& p, const GroupTok& gt, int h, i
   __syncwarp();
   if (lane == 0) {
     __threadfence();
-    last = atomicAdd(p.merge_cnt + idx, 1) == gt.pcount - 1;
+    last = atomicAdd(p.merge_cnt + idx, 1) == gt.pcount() - 1;
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
   __threadfence();
   const int poff = __ldcg(p.tok_poff + gt.tok);
   float m = -INFINITY;
-  for (int k = 0; k < gt.pcount; ++k) m = fmaxf(m, __ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h));
+  for (int k = 0; k < gt.pcount(); ++k) m = fmaxf(m, __ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h));
   float acc[EPL], den = 0.f;
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   if (m != -INFINITY) {
-    for (int k = 0; k < gt.pcount; ++k) {
+    for (int k = 0; k < gt.pcount(); ++k) {
       const size_t slot = (size_t)(poff + k) * p.hq + h;
       const float w = ptx::ex2(__ldcg(p.part_lse + slot) - m);
       den += w;
@@ -442,19 +442,22 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nr = min(RB, u.nrows);
   float qv[RB][EPL], o[RB][EPL], m[RB], l[RB];
-  int vis[RB];
+  int vis[RB], slot[RB];
 #pragma unroll
   for (int i = 0; i < RB; ++i) {
     m[i] = -INFINITY;
     l[i] = 0.f;
     vis[i] = 0;
+    slot[i] = -1;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[i][e] = qv[i][e] = 0.f;
-    if (i < nr) {
+    const GroupTok gt = i < nr ? p.gtoks[u.tok_off + (u.row0 + i) / p.gqa]
+                               : GroupTok{-1, 0, -1, 0};
+    if (gt.tok >= 0) {  // filler rows of a packed unit see nothing
       const int grow = u.row0 + i;
-      const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
       const int h = u.kvh * p.gqa + grow % p.gqa;
       vis[i] = gt.vis;
+      slot[i] = gt.slot();
       const uint16_t* src = p.q + ((size_t)gt.tok * p.hq + h) * D + lane * EPL;
       if constexpr (EPL == 4) {
         const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
@@ -486,7 +489,8 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
         const int pos = mt >> 5, nvalid = mt & 31;
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
-          const int lim = i < nr ? max(0, min(nvalid, vis[i] - pos)) : 0;
+          // a packed row sees only its own slot's page (warp bb reads page bb)
+          const int lim = (i < nr && (slot[i] < 0 || slot[i] == bb)) ? max(0, min(nvalid, vis[i] - pos)) : 0;
           if (lim == 0) continue;  // warp-uniform
           // 16 independent partial dots, then one transposed reduction:
           // lane L ends with the score of token L >> 1 of the block.
@@ -559,9 +563,11 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
         for (int e = 0; e < EPL; ++e) O[e] = fmaf(sm_o[(w * RB + i) * D + lane * EPL + e], sc, O[e]);
       }
     }
-    if (__shfl_sync(0xffffffffu, *sh.abort_flag == 0, 0)) {  // warp-uniform
+    const GroupTok gt = p.gtoks[u.tok_off + (u.row0 + i) / p.gqa];
+    // warp-uniform: the abort flag is read once per warp; filler rows of a
+    // packed unit write nothing
+    if (__shfl_sync(0xffffffffu, *sh.abort_flag == 0, 0) && gt.tok >= 0) {
       const int grow = u.row0 + i;
-      const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
       const int h = u.kvh * p.gqa + grow % p.gqa;
       const float inv = L > 0.f ? 1.f / L : 0.f;
       const float lse2 = L > 0.f ? M + __log2f(L) : -INFINITY;
@@ -570,9 +576,9 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
         dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
         if (lane == 0 && p.lse) p.lse[(size_t)gt.tok * p.hq + h] = lse2 * kLn2;
       } else {
-        const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
-        dst = p.part_o + slot * D;
-        if (lane == 0) p.part_lse[slot] = lse2;
+        const size_t ps = (size_t)(gt.pbase + u.chunk) * p.hq + h;
+        dst = p.part_o + ps * D;
+        if (lane == 0) p.part_lse[ps] = lse2;
       }
 #pragma unroll
       for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = O[e] * inv;
@@ -597,13 +603,12 @@ __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1)
 template <int D>
 __device__ __forceinline__ GroupTok prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
   const UnitDesc u = p.units[k];
-  const bool row_ok = tid < u.nrows;
   const uint16_t* src = p.q;
-  GroupTok gt{0, 0, -1, 0};
+  GroupTok gt{-1, 0, -1, 0};
+  if (tid < u.nrows) gt = p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa];
+  const bool row_ok = gt.tok >= 0;  // filler rows of a packed unit load zeros
   if (row_ok) {
-    const int grow = u.row0 + tid;
-    gt = p.gtoks[u.tok_off + grow / p.gqa];
-    const int h = u.kvh * p.gqa + grow % p.gqa;
+    const int h = u.kvh * p.gqa + (u.row0 + tid) % p.gqa;
     src = p.q + ((size_t)gt.tok * p.hq + h) * D;
   }
 #pragma unroll
@@ -646,7 +651,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
   const uint32_t qbuf = sh.base + C::kOffQ;
   const uint32_t o_tmem = tmem + lane_base + 128;
   uint32_t g = 0, gm = 0, nu = 0;
-  GroupTok gt_next{0, 0, -1, 0};  // this thread's row record in the next tensor-core unit
+  GroupTok gt_next{-1, 0, -1, 0};  // this thread's row in the next tensor-core unit
   {
     const int first = next_mma_unit(p, u0, u1);
     if (first >= 0) {
@@ -662,9 +667,10 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     if (ui + 1 < u1) un = p.units[ui + 1];
     const int T = unit_tiles(u);
     if (T == 0) {  // empty span: every row sees nothing
-      if (tid < u.nrows && !*sh.abort_flag) {
+      const GroupTok gt = tid < u.nrows ? p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa]
+                                        : GroupTok{-1, 0, -1, 0};
+      if (gt.tok >= 0 && !*sh.abort_flag) {
         const int grow = u.row0 + tid;
-        const GroupTok gt = p.gtoks[u.tok_off + grow / p.gqa];
         const int h = u.kvh * p.gqa + grow % p.gqa;
         float* dst;
         if (gt.pbase < 0) {
@@ -689,7 +695,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     const GroupTok gt_row = gt_next;
     const int vis = gt_row.vis;
     const int nxt = next_mma_unit(p, ui + 1, u1);
-    const bool row_ok = tid < u.nrows;
+    const bool row_ok = tid < u.nrows && gt_row.tok >= 0;
     const bool wact = warp * 32 < u.nrows;  // warps of padding rows keep the barriers only
     float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
     for (int j = 0; j < T; ++j) {
@@ -711,7 +717,9 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         if (bb < nb) {
           const int mt = sh.meta[s * kBpt + bb];
           partial |= (mt & 31) < 16;
-          if (row_ok) lim[bb] = max(0, min(mt & 31, vis - (mt >> 5)));
+          // a packed row sees only its own slot's page
+          if (row_ok && (gt_row.slot() < 0 || gt_row.slot() == bb))
+            lim[bb] = max(0, min(mt & 31, vis - (mt >> 5)));
         }
       }
       float sv[kTileTok];
