@@ -49,6 +49,7 @@ constexpr int kThreads = 256;
 constexpr int kComputeThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
+constexpr int kVProducerWarp = 6;
 constexpr int kComputeRegs = 200;
 constexpr int kIssueRegs = 56;
 static_assert(128 * kComputeRegs + 128 * kIssueRegs <= kThreads * 128, "register split too large");
@@ -71,9 +72,8 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffP = kOffV + kStages * kTileBytes;
   static constexpr int kOffBar = kOffP + kPBytes;
-  static constexpr int kNumBars = 2 * kStages + 13;
-  static constexpr int kOffMeta = kOffBar + kNumBars * 8 + 16;     // int [kStages][kBpt]
-  static constexpr int kOffML = kOffMeta + kStages * kBpt * 4;      // float [4][8][2]
+  static constexpr int kNumBars = 4 * kStages + 13;
+  static constexpr int kOffML = kOffBar + kNumBars * 8 + 16;  // float [4][8][2]
   // the dynamic shared window starts 1024-byte aligned (checked at start)
   static constexpr int kSmem = kOffML + 4 * kSimtTileRows * 2 * 4;
   static_assert(kSmem <= 115 * 1024, "two CTAs per SM must fit in shared memory");
@@ -91,25 +91,30 @@ struct Cfg {
 struct Shared {
   uint32_t base;  // 1024-aligned shared address of the layout
   uint8_t* ptr;
-  int* meta;      // [stage][kBpt]: span position * 32 + valid slots of each block
   volatile uint32_t* tmem_slot;
   volatile int* abort_flag;
 };
 
+// K and V of a stage have their own full / empty barriers: K is released as
+// soon as QK^T has read it, V only after P.V, so the next tiles' K streams
+// in while the current tile is still in the softmax.
 template <int D>
 struct Bars {
+  static constexpr int S = Cfg<D>::kStages;
   uint32_t b;
-  __device__ uint32_t full(int s) const { return b + 8 * s; }
-  __device__ uint32_t empty(int s) const { return b + 8 * (Cfg<D>::kStages + s); }
-  __device__ uint32_t s_full(int i) const { return b + 8 * (2 * Cfg<D>::kStages + i); }
-  __device__ uint32_t s_free(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 2 + i); }
-  __device__ uint32_t p_full() const { return b + 8 * (2 * Cfg<D>::kStages + 4); }
-  __device__ uint32_t p_empty(int i) const { return b + 8 * (2 * Cfg<D>::kStages + (i ? 11 : 5)); }
-  __device__ uint32_t o_full() const { return b + 8 * (2 * Cfg<D>::kStages + 6); }
-  __device__ uint32_t drain() const { return b + 8 * (2 * Cfg<D>::kStages + 7); }
-  __device__ uint32_t q_full(int i) const { return b + 8 * (2 * Cfg<D>::kStages + 8 + i); }
-  __device__ uint32_t never() const { return b + 8 * (2 * Cfg<D>::kStages + 10); }
-  __device__ uint32_t o_empty() const { return b + 8 * (2 * Cfg<D>::kStages + 12); }
+  __device__ uint32_t kfull(int s) const { return b + 8 * s; }
+  __device__ uint32_t kempty(int s) const { return b + 8 * (S + s); }
+  __device__ uint32_t vfull(int s) const { return b + 8 * (2 * S + s); }
+  __device__ uint32_t vempty(int s) const { return b + 8 * (3 * S + s); }
+  __device__ uint32_t s_full(int i) const { return b + 8 * (4 * S + i); }
+  __device__ uint32_t s_free(int i) const { return b + 8 * (4 * S + 2 + i); }
+  __device__ uint32_t p_full() const { return b + 8 * (4 * S + 4); }
+  __device__ uint32_t p_empty(int i) const { return b + 8 * (4 * S + (i ? 11 : 5)); }
+  __device__ uint32_t o_full() const { return b + 8 * (4 * S + 6); }
+  __device__ uint32_t drain() const { return b + 8 * (4 * S + 7); }
+  __device__ uint32_t q_full(int i) const { return b + 8 * (4 * S + 8 + i); }
+  __device__ uint32_t never() const { return b + 8 * (4 * S + 10); }
+  __device__ uint32_t o_empty() const { return b + 8 * (4 * S + 12); }
 };
 
 // Bounded wait.  Returns false (and does not wait) once the CTA has aborted;
@@ -146,13 +151,15 @@ __device__ __forceinline__ int unit_tiles(const UnitDesc& u) {
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
-// ============================================================== producer
-template <int D>
-__device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
-                         int u0, int u1, const Shared& sh, const Bars<D>& B) {
+// ============================================================== producers
+// One thread streams K (kIsV false) or V (true) of every tile of the CTA's
+// units into the stage ring.
+template <int D, bool kIsV>
+__device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int u1,
+                         const Shared& sh, const Bars<D>& B) {
   using C = Cfg<D>;
   uint32_t g = 0;
-  if (p.debug_stuck_wait) wait_bar(B.never(), 0, sh, p.err, p.wait_timeout_ns);
+  if (!kIsV && p.debug_stuck_wait) wait_bar(B.never(), 0, sh, p.err, p.wait_timeout_ns);
   uint32_t filled[C::kStages];  // 1 + tile index of the last fill issued per stage
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) filled[s] = 0;
@@ -163,30 +170,30 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     for (int b0 = u.blk0; b0 < u.blk1; b0 += kBpt, ++g) {
       const int s = g % C::kStages;
       const int nb = min(kBpt, u.blk1 - b0);
-      int2 bl[kBpt];  // all loads in flight while waiting for the stage
+      int page[kBpt];  // all loads in flight while waiting for the stage
 #pragma unroll
-      for (int bb = 0; bb < kBpt; ++bb)
-        bl[bb] = bb < nb ? __ldg(&p.blocks[b0 + bb]) : make_int2(0, 0);
+      for (int bb = 0; bb < kBpt; ++bb) page[bb] = bb < nb ? __ldg(&p.blocks[b0 + bb].x) : 0;
+      const uint32_t full = kIsV ? B.vfull(s) : B.kfull(s);
       if (g >= (uint32_t)C::kStages &&
-          !wait_bar(B.empty(s), ((g / C::kStages) + 1) & 1, sh, p.err, p.wait_timeout_ns))
+          !wait_bar(kIsV ? B.vempty(s) : B.kempty(s), ((g / C::kStages) + 1) & 1, sh, p.err,
+                    p.wait_timeout_ns))
         continue;
       if (*sh.abort_flag) continue;
-#pragma unroll
-      for (int bb = 0; bb < kBpt; ++bb) sh.meta[s * kBpt + bb] = bl[bb].y;
-      ptx::mbar_arrive_expect_tx(B.full(s), (uint32_t)nb * 2u * C::kBlockBytes);
-      const uint32_t kdst = sh.base + C::kOffK + s * C::kTileBytes;
-      const uint32_t vdst = sh.base + C::kOffV + s * C::kTileBytes;
+      ptx::mbar_arrive_expect_tx(full, (uint32_t)nb * C::kBlockBytes);
+      const uint32_t dst = sh.base + (kIsV ? C::kOffV : C::kOffK) + s * C::kTileBytes;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
         if (bb < nb) {
+          if constexpr (!kIsV) {
 #pragma unroll
-          for (int h = 0; h < C::kHalves; ++h)
-            ptx::tma_load_4d(kdst + h * (kTileTok * 128) + bb * 2048, tmk, 64 * h, 0, u.kvh,
-                             bl[bb].x, B.full(s));
-          if constexpr (D == 128)  // both 64-column halves of V in one box
-            ptx::tma_load_5d(vdst + bb * C::kBlockBytes, tmv, 0, 0, 0, u.kvh, bl[bb].x, B.full(s));
-          else
-            ptx::tma_load_4d(vdst + bb * C::kBlockBytes, tmv, 0, 0, u.kvh, bl[bb].x, B.full(s));
+            for (int h = 0; h < C::kHalves; ++h)
+              ptx::tma_load_4d(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0, u.kvh, page[bb],
+                               full);
+          } else if constexpr (D == 128) {  // both 64-column halves of V in one box
+            ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, u.kvh, page[bb], full);
+          } else {
+            ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, u.kvh, page[bb], full);
+          }
         }
       }
 #pragma unroll
@@ -198,7 +205,8 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     // let the last copy issued into every stage land before the CTA exits
 #pragma unroll
     for (int s = 0; s < C::kStages; ++s)
-      if (filled[s]) drain_wait(B.full(s), ((filled[s] - 1) / C::kStages) & 1, kDrainLimitNs);
+      if (filled[s])
+        drain_wait(kIsV ? B.vfull(s) : B.kfull(s), ((filled[s] - 1) / C::kStages) & 1, kDrainLimitNs);
   }
 }
 
@@ -229,8 +237,9 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       // the first P.V of a unit overwrites O: the previous unit's epilogue
       // must have read it
       if (jj == 0 && nu > 0) ok = wait_bar(B.o_empty(), (nu - 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
-      ptx::tc_fence_after();
       const int s = (g + jj) % C::kStages;
+      ok = ok && wait_bar(B.vfull(s), ((g + jj) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+      ptx::tc_fence_after();
       const int nbk = min(kBpt, u.blk1 - (u.blk0 + kBpt * jj));
       if (ok && !*sh.abort_flag) {
         const uint32_t vb = sh.base + C::kOffV + s * C::kTileBytes;
@@ -242,13 +251,13 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
         }
         issued = true;
       }
-      ptx::mma_commit(B.empty(s));
+      ptx::mma_commit(B.vempty(s));
       ptx::mma_commit(B.p_empty(0));
     };
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
       const int sb = (gm + j) & 1;
-      bool ok = qok && wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+      bool ok = qok && wait_bar(B.kfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
       ok = ok && wait_bar(B.s_free(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
       ptx::tc_fence_after();
       if (ok && !*sh.abort_flag) {
@@ -263,6 +272,7 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
         issued = true;
       }
       ptx::mma_commit(B.s_full(sb));
+      ptx::mma_commit(B.kempty(s));
       if (j > 0) issue_pv(j - 1);
     }
     issue_pv(T - 1);
@@ -478,15 +488,19 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
   const int inb = (EPL == 4) ? (lane & 1) * 8 : (lane & 3) * 4;
   for (int j = 0; j < T; ++j) {
     const int s = (g + j) % C::kStages;
-    const bool ok = __all_sync(
-        0xffffffffu, wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns));
     const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
+    // warp w takes page w of the tile; its record is loaded during the wait
+    const int mt_w = warp < nb ? __ldg(&p.blocks[u.blk0 + kBpt * j + warp].y) : 0;
+    const uint32_t ph = ((g + j) / C::kStages) & 1;
+    const bool ok = __all_sync(0xffffffffu, wait_bar(B.kfull(s), ph, sh, p.err, p.wait_timeout_ns) &&
+                                                wait_bar(B.vfull(s), ph, sh, p.err, p.wait_timeout_ns));
     const uint8_t* kst = sh.ptr + C::kOffK + s * C::kTileBytes + half * (kTileTok * 128) + inb;
     const uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes + half * 2048 + inb;
-    if (ok) {
-      for (int bb = warp; bb < nb; bb += 4) {
-        const int mt = sh.meta[s * kBpt + bb];
-        const int pos = mt >> 5, nvalid = mt & 31;
+    static_assert(kBpt == kComputeThreads / 32, "one page per compute warp");
+    if (ok && warp < nb) {
+      {
+        const int bb = warp;
+        const int pos = mt_w >> 5, nvalid = mt_w & 31;
 #pragma unroll
         for (int i = 0; i < RB; ++i) {
           // a packed row sees only its own slot's page (warp bb reads page bb)
@@ -530,7 +544,10 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
       }
     }
     ptx::named_bar_sync(1, kComputeThreads);
-    if (tid == 0) ptx::mbar_arrive(B.empty(s));
+    if (tid == 0) {
+      ptx::mbar_arrive(B.kempty(s));
+      ptx::mbar_arrive(B.vempty(s));
+    }
   }
   // combine the four warps' states (scratch in the P buffer, idle here)
   float* sm_o = reinterpret_cast<float*>(sh.ptr + C::kOffP);   // [4][RB][D]
@@ -697,80 +714,136 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     const int nxt = next_mma_unit(p, ui + 1, u1);
     const bool row_ok = tid < u.nrows && gt_row.tok >= 0;
     const bool wact = warp * 32 < u.nrows;  // warps of padding rows keep the barriers only
-    float m_run = -INFINITY, l_run = 0.f, l_exact = 0.f;
+    const bool packed = gt_row.slot() >= 0;  // warp w holds slot w's rows
+    float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
       const int sb = (gm + j) & 1;
-      bool ok = wait_bar(B.full(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
-      ok = ok && wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
+      // the tile's page records (span position * 32 + valid slots), loaded
+      // while S is computed
+      const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
+      const int2* blk = p.blocks + u.blk0 + kBpt * j;
+      int mt[kBpt];
+#pragma unroll
+      for (int bb = 0; bb < kBpt; ++bb) mt[bb] = bb < nb ? __ldg(&blk[bb].y) : 16;
+      const int mt_p = packed ? __ldg(&blk[warp].y) : 0;  // packed tiles hold kBpt pages
+      bool ok = wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
       // every QK^T of this unit has completed once the last S is ready: the
       // query buffer is free, so the next unit's query tile starts streaming
       if (j == T - 1 && nxt >= 0) gt_next = prefetch_q<D>(p, nxt, qbuf, tid);
-      const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
+      // Visible columns of this row in each page of the tile.  In a packed
+      // unit warp w is slot w and sees only page w of every tile.
       int lim[kBpt];
-      bool partial = false;
+      bool partial = false, full = nb == kBpt;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
         lim[bb] = 0;
         if (bb < nb) {
-          const int mt = sh.meta[s * kBpt + bb];
-          partial |= (mt & 31) < 16;
-          // a packed row sees only its own slot's page
-          if (row_ok && (gt_row.slot() < 0 || gt_row.slot() == bb))
-            lim[bb] = max(0, min(mt & 31, vis - (mt >> 5)));
+          partial |= (mt[bb] & 31) < 16;
+          if (row_ok && !packed) lim[bb] = max(0, min(mt[bb] & 31, vis - (mt[bb] >> 5)));
         }
+        full = full && (!row_ok || lim[bb] == 16);
       }
-      float sv[kTileTok];
-      if (ok && wact) {
-#pragma unroll
-        for (int c = 0; c < kTileTok / 32; ++c) {
-          float t32[32];
-          ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + c * 32, t32);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t32[e];
-        }
-        ptx::tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(B.s_free(sb));
-      // masked row max, eight independent chains; masked scores select -inf
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kTileTok; ++c)
-        mx8[c & 7] = fmaxf(mx8[c & 7], (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
-      float m_new = m_run, alpha = 1.f;
-      if (wact && mx > m_run + kRescaleLog2) {
-        m_new = mx;
-        alpha = ptx::ex2(m_run - m_new);
-      }
-      // P rounds to bf16 for the tensor cores; O is normalised by the sum of
-      // the rounded weights (the weights the MMA used), lse by the exact sum.
+      const int lim_p = packed && row_ok ? max(0, min(mt_p & 31, vis - (mt_p >> 5))) : 0;
+      float m_new = m_run, alpha = 1.f, lsum = 0.f;
       uint32_t pk[kTileTok / 2];
-      float ps4[4] = {0.f, 0.f, 0.f, 0.f}, pe4[4] = {0.f, 0.f, 0.f, 0.f};
-      if (wact) {
+      // P rounds to bf16 for the tensor cores; the row sum is kept exact in
+      // fp32 and normalises both O and the lse.
+      if (packed) {
+        float sv[16];
+        if (ok && wact) {
+          ptx::tmem_ld16(tmem + lane_base + sb * kTileTok + warp * 16, sv);
+          ptx::tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int c = 0; c < kTileTok; c += 2) {
-          const float xa = (c & 15) < lim[c >> 4] ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY;
-          const float xb =
-              ((c + 1) & 15) < lim[(c + 1) >> 4] ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY;
-          const float a = ptx::ex2(xa);
-          const float b = ptx::ex2(xb);
+          for (int c = 0; c < 16; ++c) sv[c] = 0.f;
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(B.s_free(sb));
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 16; ++c) m4[c & 3] = fmaxf(m4[c & 3], c < lim_p ? sv[c] : -INFINITY);
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+        if (wact && mx > m_run + kRescaleLog2) {
+          m_new = mx;
+          alpha = ptx::ex2(m_run - m_new);
+        }
+        float e4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 16; c += 2) {
+          const float a = ptx::ex2(c < lim_p ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY);
+          const float b = ptx::ex2(c + 1 < lim_p ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY);
           pk[c >> 1] = ptx::pack_bf16(a, b);
-          ps4[(c >> 1) & 3] += bf16_lo(pk[c >> 1]) + bf16_hi(pk[c >> 1]);
-          pe4[(c >> 1) & 3] += a + b;
+          e4[(c >> 1) & 3] += a + b;
+        }
+        lsum = (e4[0] + e4[1]) + (e4[2] + e4[3]);
+      } else {
+        // a warp whose rows all see the whole tile skips the masks
+        const bool fast = __all_sync(0xffffffffu, full);
+        float sv[kTileTok];
+        if (ok && wact) {
+#pragma unroll
+          for (int c = 0; c < kTileTok / 32; ++c) {
+            float t32[32];
+            ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + c * 32, t32);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t32[e];
+          }
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(B.s_free(sb));
+        // row max over the visible columns; masked scores select -inf
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (fast) {
+#pragma unroll
+          for (int c = 0; c < kTileTok; c += 2)
+            m4[(c >> 1) & 3] = ptx::max3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTileTok; ++c)
+            m4[c & 3] = fmaxf(m4[c & 3], (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY);
+        }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+        if (wact && mx > m_run + kRescaleLog2) {
+          m_new = mx;
+          alpha = ptx::ex2(m_run - m_new);
+        }
+        if (wact && fast) {
+          const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(-m_new, -m_new);
+          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // (0.f, 0.f) pairs
+#pragma unroll
+          for (int c = 0; c < kTileTok; c += 2) {
+            float xa, xb;
+            ptx::f2_split(ptx::fma_f32x2(ptx::f2(sv[c], sv[c + 1]), sc2, nm2), xa, xb);
+            const float a = ptx::ex2(xa), b = ptx::ex2(xb);
+            pk[c >> 1] = ptx::pack_bf16(a, b);
+            acc[(c >> 1) & 3] = ptx::add_f32x2(acc[(c >> 1) & 3], ptx::f2(a, b));
+          }
+          float e8[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) ptx::f2_split(acc[k], e8[2 * k], e8[2 * k + 1]);
+          lsum = ((e8[0] + e8[1]) + (e8[2] + e8[3])) + ((e8[4] + e8[5]) + (e8[6] + e8[7]));
+        } else if (wact) {
+          float e4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < kTileTok; c += 2) {
+            const float xa = (c & 15) < lim[c >> 4] ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY;
+            const float xb =
+                ((c + 1) & 15) < lim[(c + 1) >> 4] ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY;
+            const float a = ptx::ex2(xa), b = ptx::ex2(xb);
+            pk[c >> 1] = ptx::pack_bf16(a, b);
+            e4[(c >> 1) & 3] += a + b;
+          }
+          lsum = (e4[0] + e4[1]) + (e4[2] + e4[3]);
         }
       }
-      l_run = fmaf(l_run, alpha, (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
-      l_exact = fmaf(l_exact, alpha, (pe4[0] + pe4[1]) + (pe4[2] + pe4[3]));
+      l_run = fmaf(l_run, alpha, lsum);
       m_run = m_new;
       // the P buffer and O are free once the previous P.V has completed
       ok = wait_bar(B.p_empty(0), (gm + j + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
@@ -790,21 +863,35 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       }
       if (wact) {
         const uint32_t pb = sh.base + C::kOffP;
+        if (packed) {
+          // this warp's page is P columns [16w, 16w + 16); its other columns
+          // stay zero for the whole unit
+          ptx::st_shared_v4(pb + sw128(tid, 2 * warp), pk[0], pk[1], pk[2], pk[3]);
+          ptx::st_shared_v4(pb + sw128(tid, 2 * warp + 1), pk[4], pk[5], pk[6], pk[7]);
+          if (j == 0) {
 #pragma unroll
-        for (int c = 0; c < kTileTok / 8; ++c)
-          ptx::st_shared_v4(pb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), pk[4 * c], pk[4 * c + 1],
-                            pk[4 * c + 2], pk[4 * c + 3]);
+            for (int c = 0; c < kTileTok / 8; ++c)
+              if ((c >> 1) != warp) ptx::st_shared_v4(pb + sw128(tid, c), 0u, 0u, 0u, 0u);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTileTok / 8; ++c)
+            ptx::st_shared_v4(pb + sw128(tid, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
       }
-      if (partial) {
+      if (partial &&
+          wait_bar(B.vfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns)) {
         // zero the V rows of page slots that hold no token (they may hold
         // anything; P is 0 there but 0 * NaN is not 0)
         uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes;
-        for (int idx = tid; idx < nb * 16 * C::kHalves * 8; idx += kComputeThreads) {
-          const int ch = idx & 7, r = (idx >> 3) % (nb * 16), hh = (idx >> 3) / (nb * 16);
-          const int nvalid = sh.meta[s * kBpt + (r >> 4)] & 31;
-          if ((r & 15) >= nvalid)
-            *reinterpret_cast<uint4*>(vst + (r >> 4) * C::kBlockBytes + hh * 2048 + (r & 15) * 128 +
-                                      ch * 16) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int bb = 0; bb < kBpt; ++bb) {
+          const int nv = mt[bb] & 31;
+          for (int idx = tid; idx < (16 - nv) * 8 * C::kHalves; idx += kComputeThreads) {
+            const int r = nv + idx / (8 * C::kHalves), hh = (idx >> 3) % C::kHalves, ch = idx & 7;
+            *reinterpret_cast<uint4*>(vst + bb * C::kBlockBytes + hh * 2048 + r * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
         }
       }
       ptx::fence_proxy_async_smem();
@@ -824,7 +911,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     ptx::tc_fence_after();
     if (ok && wact) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse2 = l_exact > 0.f ? m_run + __log2f(l_exact) : -INFINITY;
+      const float lse2 = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float t32[32];
@@ -860,14 +947,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   Bars<D> B{sh.base + C::kOffBar};
   sh.tmem_slot = reinterpret_cast<volatile uint32_t*>(sh.ptr + C::kOffBar + C::kNumBars * 8);
   sh.abort_flag = reinterpret_cast<volatile int*>(sh.ptr + C::kOffBar + C::kNumBars * 8 + 4);
-  sh.meta = reinterpret_cast<int*>(sh.ptr + C::kOffMeta);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u0 = p.cta_off[blockIdx.x], u1 = p.cta_off[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(B.full(s), 1);
-      ptx::mbar_init(B.empty(s), 1);
+      ptx::mbar_init(B.kfull(s), 1);
+      ptx::mbar_init(B.kempty(s), 1);
+      ptx::mbar_init(B.vfull(s), 1);
+      ptx::mbar_init(B.vempty(s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(B.s_full(i), 1);
@@ -912,10 +1000,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else {
     ptx::setmaxnreg_dec<kIssueRegs>();
     if (warp == kProducerWarp) {
-      if (lane == 0) producer<D>(&tmk, &tmv, p, u0, u1, sh, B);
+      if (lane == 0) producer<D, false>(&tmk, p, u0, u1, sh, B);
     } else if (warp == kMmaWarp) {
       if (lane == 0) mma_issuer<D>(p, u0, u1, sh, B, tmem);
-    }  // warps 6 and 7 only complete the warpgroup
+    } else if (warp == kVProducerWarp) {
+      if (lane == 0) producer<D, true>(&tmv, p, u0, u1, sh, B);
+    }  // warp 7 only completes the warpgroup
     __syncwarp();
   }
   ptx::tc_fence_before();
