@@ -486,11 +486,16 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
   const int half = (EPL == 4) ? (lane >> 4) : 0;
   const int chunk = (EPL == 4) ? ((lane & 15) >> 1) : (lane >> 2);
   const int inb = (EPL == 4) ? (lane & 1) * 8 : (lane & 3) * 4;
+  int mt_next = warp < min(kBpt, u.blk1 - u.blk0) ? __ldg(&p.blocks[u.blk0 + warp].y) : 0;
   for (int j = 0; j < T; ++j) {
     const int s = (g + j) % C::kStages;
     const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
-    // warp w takes page w of the tile; its record is loaded during the wait
-    const int mt_w = warp < nb ? __ldg(&p.blocks[u.blk0 + kBpt * j + warp].y) : 0;
+    // warp w takes page w of the tile; the next tile's record is loaded now
+    const int mt_w = mt_next;
+    if (j + 1 < T) {
+      const int nbn = min(kBpt, u.blk1 - (u.blk0 + kBpt * (j + 1)));
+      mt_next = warp < nbn ? __ldg(&p.blocks[u.blk0 + kBpt * (j + 1) + warp].y) : 0;
+    }
     const uint32_t ph = ((g + j) / C::kStages) & 1;
     const bool ok = __all_sync(0xffffffffu, wait_bar(B.kfull(s), ph, sh, p.err, p.wait_timeout_ns) &&
                                                 wait_bar(B.vfull(s), ph, sh, p.err, p.wait_timeout_ns));
@@ -716,17 +721,21 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     const bool wact = warp * 32 < u.nrows;  // warps of padding rows keep the barriers only
     const bool packed = gt_row.slot() >= 0;  // warp w holds slot w's rows
     float m_run = -INFINITY, l_run = 0.f;
+    // the tiles' page records (span position * 32 + valid slots), each
+    // loaded one tile ahead; packed tiles always hold kBpt pages
+    int mt[kBpt], mt_p;
+    auto load_records = [&](int jt) {
+      const int nbt = min(kBpt, u.blk1 - (u.blk0 + kBpt * jt));
+      const int2* blk = p.blocks + u.blk0 + kBpt * jt;
+#pragma unroll
+      for (int bb = 0; bb < kBpt; ++bb) mt[bb] = bb < nbt ? __ldg(&blk[bb].y) : 16;
+      mt_p = packed ? __ldg(&blk[warp].y) : 0;
+    };
+    load_records(0);
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
       const int sb = (gm + j) & 1;
-      // the tile's page records (span position * 32 + valid slots), loaded
-      // while S is computed
       const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
-      const int2* blk = p.blocks + u.blk0 + kBpt * j;
-      int mt[kBpt];
-#pragma unroll
-      for (int bb = 0; bb < kBpt; ++bb) mt[bb] = bb < nb ? __ldg(&blk[bb].y) : 16;
-      const int mt_p = packed ? __ldg(&blk[warp].y) : 0;  // packed tiles hold kBpt pages
       bool ok = wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
@@ -747,6 +756,10 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         full = full && (!row_ok || lim[bb] == 16);
       }
       const int lim_p = packed && row_ok ? max(0, min(mt_p & 31, vis - (mt_p >> 5))) : 0;
+      int nvalid = 0;  // valid slots of the tile's pages, 5 bits each
+#pragma unroll
+      for (int bb = 0; bb < kBpt; ++bb) nvalid |= (mt[bb] & 31) << (5 * bb);
+      if (j + 1 < T) load_records(j + 1);
       float m_new = m_run, alpha = 1.f, lsum = 0.f;
       uint32_t pk[kTileTok / 2];
       // P rounds to bf16 for the tensor cores; the row sum is kept exact in
@@ -886,7 +899,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes;
 #pragma unroll
         for (int bb = 0; bb < kBpt; ++bb) {
-          const int nv = mt[bb] & 31;
+          const int nv = (nvalid >> (5 * bb)) & 31;
           for (int idx = tid; idx < (16 - nv) * 8 * C::kHalves; idx += kComputeThreads) {
             const int r = nv + idx / (8 * C::kHalves), hh = (idx >> 3) % C::kHalves, ch = idx & 7;
             *reinterpret_cast<uint4*>(vst + bb * C::kBlockBytes + hh * 2048 + r * 128 + ch * 16) =
