@@ -77,8 +77,9 @@ typedef struct {
   int32_t ts_q_set[4];      /* [16,64,128] query tile sizes of the cost model;
                                zero entries end the list                     */
   int32_t ts_c;             /* [64] context tile size of the cost model      */
-  int32_t mma_min_rows;     /* [4] rows per kv head from which a group runs
-                               on tensor cores; fewer run on CUDA cores      */
+  int32_t mma_min_rows;     /* [1] rows per kv head from which a group runs
+                               on tensor cores; fewer run on CUDA cores
+                               (thin groups are packed four to a tile)      */
   int32_t split_tokens;     /* [0 = automatic] chunk length for splitting
                                long spans; < 0 disables splitting            */
   int32_t min_split_tokens; /* [256] smallest automatic chunk               */

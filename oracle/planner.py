@@ -39,7 +39,7 @@ class PlannerOptions:
     beta: int = 0                        # optional SplitQ duplicate-KV weight
     ts_q_set: tuple = (16, 64, 128)      # query tile sizes (multi-stage tiling)
     ts_c: int = 64                       # context tile size
-    mma_min_rows: int = 4                # rows per kv head to use tensor cores
+    mma_min_rows: int = 1                # rows per kv head to use tensor cores
     mma_tile_rows: int = 128             # MMA query tile (M)
     simt_tile_rows: int = 8              # CUDA-core query tile
     kv_tile_tokens: int = 64             # chunk granularity (tokens)

@@ -39,7 +39,7 @@ struct Options {
   int64_t beta = 0;
   std::vector<int32_t> ts_q{16, 64, 128};
   int32_t ts_c = 64;
-  int32_t mma_min_rows = 4;
+  int32_t mma_min_rows = 1;
   int32_t split_tokens = 0;
   int32_t min_split_tokens = 256;
   int32_t split_waves = 4;

@@ -1,19 +1,21 @@
 // Persistent grouped partial-attention kernel for sm_103a.
 //
-// One CTA per SM walks its list of work units (group, kv head, query tile,
-// chunk).  A unit's KV span is streamed once, 128 tokens (8 pages) per tile,
-// by TMA into a ring of shared-memory stages (128-byte swizzle, one box per
-// page and 64-column half).  The tile is consumed on one of two paths:
+// Two CTAs per SM each walk their list of work units (group, kv head, query
+// tile, chunk).  A unit's KV span is streamed once, 64 tokens (4 pages) per
+// tile, by TMA into rings of shared-memory stages (128-byte swizzle; K and V
+// have their own rings).  The tile is consumed on one of two paths:
 //
 //  * tensor cores (stacked query rows; FastTree review page, "高效树结构注意力
 //    内核设计": GEMV becomes GEMM once a group's queries are stacked): the
-//    group's query tile (128 rows = query tokens x GQA heads) sits in shared
-//    memory; S = Q K^T goes to TMEM (double-buffered), the four compute warps
-//    read one row per thread, apply the mask and an online softmax (the
-//    running max is raised only when it grows by more than 2^8, so O is
-//    rarely rescaled), write P as bf16 to shared memory, and tcgen05 adds
-//    P V into the O accumulator in TMEM.
-//  * CUDA cores (thin groups): the compute warps split the tile's pages,
+//    group's query tile (128 rows = query tokens x GQA heads; or four thin
+//    groups packed one per warp) sits in shared memory; S = Q K^T goes to
+//    TMEM (double-buffered), the four compute warps read one row per thread,
+//    apply the mask and an online softmax (the running max is raised only
+//    when it grows by more than 2^8, so O is rarely rescaled), write P as
+//    bf16 to shared memory, and tcgen05 adds P V into the O accumulator in
+//    TMEM.
+//  * CUDA cores (groups below the tensor-core row threshold, when it is
+//    raised): the compute warps split the tile's pages,
 //    lanes split the head dimension, and each warp keeps its own online
 //    softmax; the warps' states are combined at the end of the unit.
 //
@@ -22,7 +24,8 @@
 // notes page, "Tree-Topology-Aware Global Reduction Strategy").
 //
 // Roles: warps 0-3 compute (thread i owns TMEM lane / query row i), warp 4
-// issues TMA, warp 5 owns TMEM and issues tcgen05.mma.  Every wait is
+// streams K and warp 6 streams V by TMA, warp 5 owns TMEM and issues
+// tcgen05.mma.  Every wait is
 // bounded: if one runs out the CTA records TA_DEVERR_TIMEOUT, stops issuing
 // work, waits (bounded) for its copies and MMAs in flight, frees TMEM and
 // returns.
