@@ -75,7 +75,7 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffP = kOffV + kStages * kTileBytes;
   static constexpr int kOffBar = kOffP + kPBytes;
-  static constexpr int kNumBars = 4 * kStages + 13;
+  static constexpr int kNumBars = 4 * kStages + 12;
   static constexpr int kOffML = kOffBar + kNumBars * 8 + 16;  // float [4][8][2]
   // the dynamic shared window starts 1024-byte aligned (checked at start)
   static constexpr int kSmem = kOffML + 4 * kSimtTileRows * 2 * 4;
@@ -109,15 +109,15 @@ struct Bars {
   __device__ uint32_t kempty(int s) const { return b + 8 * (S + s); }
   __device__ uint32_t vfull(int s) const { return b + 8 * (2 * S + s); }
   __device__ uint32_t vempty(int s) const { return b + 8 * (3 * S + s); }
+  // S buffer i: S ready / its P consumed by P.V / its P written
   __device__ uint32_t s_full(int i) const { return b + 8 * (4 * S + i); }
-  __device__ uint32_t s_free(int i) const { return b + 8 * (4 * S + 2 + i); }
-  __device__ uint32_t p_full() const { return b + 8 * (4 * S + 4); }
-  __device__ uint32_t p_empty(int i) const { return b + 8 * (4 * S + (i ? 11 : 5)); }
+  __device__ uint32_t pv_done(int i) const { return b + 8 * (4 * S + 2 + i); }
+  __device__ uint32_t p_full(int i) const { return b + 8 * (4 * S + 4 + i); }
   __device__ uint32_t o_full() const { return b + 8 * (4 * S + 6); }
   __device__ uint32_t drain() const { return b + 8 * (4 * S + 7); }
   __device__ uint32_t q_full(int i) const { return b + 8 * (4 * S + 8 + i); }
   __device__ uint32_t never() const { return b + 8 * (4 * S + 10); }
-  __device__ uint32_t o_empty() const { return b + 8 * (4 * S + 12); }
+  __device__ uint32_t o_empty() const { return b + 8 * (4 * S + 11); }
 };
 
 // Bounded wait.  Returns false (and does not wait) once the CTA has aborted;
@@ -220,7 +220,6 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
   using C = Cfg<D>;
   uint32_t g = 0, gm = 0, nu = 0;
   const uint32_t qbase = sh.base + C::kOffQ;
-  const uint32_t pbase = sh.base + C::kOffP;
   bool issued = false;
   UnitDesc un = u0 < u1 ? p.units[u0] : UnitDesc{};
   for (int ui = u0; ui < u1; ++ui) {
@@ -236,7 +235,8 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
     const uint32_t qb = qbase;
     const uint32_t o_tmem = tmem + 128;
     auto issue_pv = [&](int jj) {
-      bool ok = wait_bar(B.p_full(), (gm + jj) & 1, sh, p.err, p.wait_timeout_ns);
+      const int pb = (gm + jj) & 1;  // P(jj) sits in the first 32 columns of S buffer pb
+      bool ok = wait_bar(B.p_full(pb), ((gm + jj) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
       // the first P.V of a unit overwrites O: the previous unit's epilogue
       // must have read it
       if (jj == 0 && nu > 0) ok = wait_bar(B.o_empty(), (nu - 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
@@ -246,22 +246,22 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       const int nbk = min(kBpt, u.blk1 - (u.blk0 + kBpt * jj));
       if (ok && !*sh.abort_flag) {
         const uint32_t vb = sh.base + C::kOffV + s * C::kTileBytes;
-        const uint32_t pb = pbase;
-        for (int kk = 0; kk < nbk; ++kk) {
-          const uint64_t ad = ptx::sdesc_sw128(pb + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+        for (int kk = 0; kk < nbk; ++kk) {  // one page (16 tokens = 8 columns of P) per MMA
           const uint64_t bd = ptx::sdesc_sw128(vb + kk * C::kBlockBytes, 2048, 1024);
-          ptx::mma_bf16(o_tmem, ad, bd, C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_bf16_ts(o_tmem, tmem + pb * kTileTok + kk * 8, bd, C::kIdescPV,
+                           (jj > 0 || kk > 0) ? 1u : 0u);
         }
         issued = true;
       }
       ptx::mma_commit(B.vempty(s));
-      ptx::mma_commit(B.p_empty(0));
+      ptx::mma_commit(B.pv_done(pb));
     };
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
       const int sb = (gm + j) & 1;
       bool ok = qok && wait_bar(B.kfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
-      ok = ok && wait_bar(B.s_free(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
+      // S buffer sb holds P of the tile two back until that P.V has completed
+      ok = ok && wait_bar(B.pv_done(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
       ptx::tc_fence_after();
       if (ok && !*sh.abort_flag) {
         const uint32_t kb = sh.base + C::kOffK + s * C::kTileBytes;
@@ -776,8 +776,6 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 #pragma unroll
           for (int c = 0; c < 16; ++c) sv[c] = 0.f;
         }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(B.s_free(sb));
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < 16; ++c) m4[c & 3] = fmaxf(m4[c & 3], c < lim_p ? sv[c] : -INFINITY);
@@ -812,8 +810,6 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 #pragma unroll
           for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
         }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(B.s_free(sb));
         // row max over the visible columns; masked scores select -inf
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (fast) {
@@ -861,11 +857,11 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       }
       l_run = fmaf(l_run, alpha, lsum);
       m_run = m_new;
-      // the P buffer and O are free once the previous P.V has completed
-      ok = wait_bar(B.p_empty(0), (gm + j + 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
-      ok = __all_sync(0xffffffffu, ok);
-      ptx::tc_fence_after();
-      if (ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // a rescale of O waits until O holds the previous tile's P.V
+      if (ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f) &&
+          __all_sync(0xffffffffu, wait_bar(B.pv_done((gm + j - 1) & 1), ((gm + j - 1) >> 1) & 1, sh,
+                                           p.err, p.wait_timeout_ns))) {
+        ptx::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float t32[32];
@@ -877,23 +873,20 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         }
         ptx::tmem_wait_st();
       }
-      if (wact) {
-        const uint32_t pb = sh.base + C::kOffP;
+      // P (bf16 pairs, 32 columns) replaces S in the first half of its TMEM
+      // buffer; the S values were read above
+      if (ok && wact) {
+        const uint32_t pt = tmem + lane_base + sb * kTileTok;
         if (packed) {
-          // this warp's page is P columns [16w, 16w + 16); its other columns
-          // stay zero for the whole unit
-          ptx::st_shared_v4(pb + sw128(tid, 2 * warp), pk[0], pk[1], pk[2], pk[3]);
-          ptx::st_shared_v4(pb + sw128(tid, 2 * warp + 1), pk[4], pk[5], pk[6], pk[7]);
-          if (j == 0) {
+          // this warp's page is P columns [8w, 8w + 8); the rest is zero
+          uint32_t pw[kTileTok / 2];
 #pragma unroll
-            for (int c = 0; c < kTileTok / 8; ++c)
-              if ((c >> 1) != warp) ptx::st_shared_v4(pb + sw128(tid, c), 0u, 0u, 0u, 0u);
-          }
+          for (int c = 0; c < kTileTok / 2; ++c) pw[c] = (c >> 3) == warp ? pk[c & 7] : 0u;
+          ptx::tmem_st32u(pt, pw);
         } else {
-#pragma unroll
-          for (int c = 0; c < kTileTok / 8; ++c)
-            ptx::st_shared_v4(pb + sw128(tid, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          ptx::tmem_st32u(pt, pk);
         }
+        ptx::tmem_wait_st();
       }
       if (partial &&
           wait_bar(B.vfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns)) {
@@ -910,9 +903,9 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
           }
         }
       }
-      ptx::fence_proxy_async_smem();
+      if (partial) ptx::fence_proxy_async_smem();  // the zeroed V rows
       ptx::tc_fence_before();
-      ptx::mbar_arrive(B.p_full());
+      ptx::mbar_arrive(B.p_full(sb));
     }
     // hand the next unit's query tile to the MMA issuer, so its first QK^T
     // overlaps this unit's epilogue
@@ -975,11 +968,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(B.s_full(i), 1);
-      ptx::mbar_init(B.s_free(i), kComputeThreads);
+      ptx::mbar_init(B.pv_done(i), 1);
+      // one per S buffer: a warp may arrive for tile t + 1 before the others
+      // arrive for tile t, and only tile t + 2 (same buffer) waits for P.V(t)
+      ptx::mbar_init(B.p_full(i), kComputeThreads);
     }
-    ptx::mbar_init(B.p_full(), kComputeThreads);
-    ptx::mbar_init(B.p_empty(0), 1);
-    ptx::mbar_init(B.p_empty(1), 1);
     ptx::mbar_init(B.q_full(0), kComputeThreads);
     ptx::mbar_init(B.q_full(1), kComputeThreads);
     ptx::mbar_init(B.o_full(), 1);
