@@ -622,25 +622,35 @@ __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1)
   return -1;
 }
 
-// Start copying unit k's query tile (row tid; zeros past its rows) into the
-// swizzled buffer at qb.  Completion: cp_async_wait_all().  Returns the row's
-// record (token, visible end, partial slot); vis = 0 past the unit's rows.
+// Row tid of unit k's query tile: its record (token, visible end, partial
+// slot; token -1 past the unit's rows and for filler rows of a packed unit)
+// and the start of its query row.  Looked up a unit ahead: the tables are
+// usually out of L2 by then.
+struct QRow {
+  GroupTok gt;
+  const uint16_t* src;
+};
 template <int D>
-__device__ __forceinline__ GroupTok prefetch_q(const AttnParams& p, int k, uint32_t qb, int tid) {
+__device__ __forceinline__ QRow q_row(const AttnParams& p, int k, int tid) {
   const UnitDesc u = p.units[k];
-  const uint16_t* src = p.q;
-  GroupTok gt{-1, 0, -1, 0};
-  if (tid < u.nrows) gt = p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa];
-  const bool row_ok = gt.tok >= 0;  // filler rows of a packed unit load zeros
-  if (row_ok) {
+  QRow r{GroupTok{-1, 0, -1, 0}, p.q};
+  if (tid < u.nrows) r.gt = p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa];
+  if (r.gt.tok >= 0) {
     const int h = u.kvh * p.gqa + (u.row0 + tid) % p.gqa;
-    src = p.q + ((size_t)gt.tok * p.hq + h) * D;
+    r.src = p.q + ((size_t)r.gt.tok * p.hq + h) * D;
   }
+  return r;
+}
+
+// Start copying a query row into row tid of the swizzled buffer at qb (zeros
+// for a row without a token).  Completion: cp_async_wait_all().
+template <int D>
+__device__ __forceinline__ void load_q(const QRow& r, uint32_t qb, int tid) {
+  const uint32_t n = r.gt.tok >= 0 ? 16u : 0u;
 #pragma unroll
   for (int c = 0; c < D / 8; ++c)
-    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), src + c * 8, row_ok ? 16u : 0u);
+    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), r.src + c * 8, n);
   ptx::cp_async_commit();
-  return gt;
 }
 
 // Write columns [c0, c0 + N) of row `grow`'s result (normalised O, and lse
@@ -680,7 +690,9 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
   {
     const int first = next_mma_unit(p, u0, u1);
     if (first >= 0) {
-      gt_next = prefetch_q<D>(p, first, qbuf, tid);
+      const QRow r = q_row<D>(p, first, tid);
+      load_q<D>(r, qbuf, tid);
+      gt_next = r.gt;
       ptx::cp_async_wait_all();
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(B.q_full(0));
@@ -720,6 +732,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     const GroupTok gt_row = gt_next;
     const int vis = gt_row.vis;
     const int nxt = next_mma_unit(p, ui + 1, u1);
+    const QRow q_next = nxt >= 0 ? q_row<D>(p, nxt, tid) : QRow{GroupTok{-1, 0, -1, 0}, p.q};
     const bool row_ok = tid < u.nrows && gt_row.tok >= 0;
     const bool wact = warp * 32 < u.nrows;  // warps of padding rows keep the barriers only
     const bool packed = gt_row.slot() >= 0;  // warp w holds slot w's rows
@@ -739,14 +752,9 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       const int s = (g + j) % C::kStages;
       const int sb = (gm + j) & 1;
       const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
-      bool ok = wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      ptx::tc_fence_after();
-      // every QK^T of this unit has completed once the last S is ready: the
-      // query buffer is free, so the next unit's query tile starts streaming
-      if (j == T - 1 && nxt >= 0) gt_next = prefetch_q<D>(p, nxt, qbuf, tid);
-      // Visible columns of this row in each page of the tile.  In a packed
-      // unit warp w is slot w and sees only page w of every tile.
+      // Visible columns of this row in each page of the tile (decoded while
+      // QK^T may still run).  In a packed unit warp w is slot w and sees
+      // only page w of every tile.
       int lim[kBpt];
       bool partial = false, full = nb == kBpt;
 #pragma unroll
@@ -763,6 +771,15 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) nvalid |= (mt[bb] & 31) << (5 * bb);
       if (j + 1 < T) load_records(j + 1);
+      bool ok = wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      ptx::tc_fence_after();
+      // every QK^T of this unit has completed once the last S is ready: the
+      // query buffer is free, so the next unit's query tile starts streaming
+      if (j == T - 1 && nxt >= 0) {
+        load_q<D>(q_next, qbuf, tid);
+        gt_next = q_next.gt;
+      }
       float m_new = m_run, alpha = 1.f, lsum = 0.f;
       uint32_t pk[kTileTok / 2];
       // P rounds to bf16 for the tensor cores; the row sum is kept exact in
