@@ -14,12 +14,14 @@ namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// One warp per (merge token, q head).  Lane k reads lse of partial k (the
-// common case has fewer than 32 partials), then the partials' rows are read
-// four at a time so their loads are in flight together.
+// One warp per (merge token, q head).  The partials are read eight at a time
+// (lse and the lane's columns of every O row in flight together) and folded
+// online: the running max M only grows, and the sums kept so far are scaled
+// by 2^(M_old - M_new) when it does.
 template <int D>
-__global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(256, 4) lse_merge_kernel(const MergeParams p) {
   constexpr int EPL = D / 32;  // 4 or 2 columns per lane
+  constexpr int G = 8;         // partials per round
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -28,45 +30,47 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
     const MergeItem it = p.items[idx / p.hq];
     const int h = idx % p.hq;
     const float* lse_h = p.part_lse + (size_t)it.poff * p.hq + h;  // partial k at lse_h[k * hq]
-    float M = -INFINITY;
-    for (int k = lane; k < it.count; k += 32) M = fmaxf(M, __ldcg(lse_h + (size_t)k * p.hq));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float acc[EPL], den = 0.f;
+    const float* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + lane * EPL;
+    float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    if (M != -INFINITY) {
-      const float* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + lane * EPL;
-      for (int k0 = 0; k0 < it.count; k0 += 4) {
-        float w[4], v[4][EPL];
+    for (int k0 = 0; k0 < it.count; k0 += G) {
+      float w[G], v[G][EPL];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int k = k0 + q;
-          w[q] = 0.f;
+      for (int q = 0; q < G; ++q) {
+        const int k = k0 + q;
+        w[q] = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) v[q][e] = 0.f;
-          if (k < it.count) {
-            w[q] = __ldcg(lse_h + (size_t)k * p.hq);
-            const float* src = o_h + (size_t)k * p.hq * D;
-            if constexpr (EPL == 4) {
-              const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-              v[q][0] = t.x, v[q][1] = t.y, v[q][2] = t.z, v[q][3] = t.w;
-            } else {
-              const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-              v[q][0] = t.x, v[q][1] = t.y;
-            }
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (k0 + q < it.count) {
-            const float wq = exp2f(w[q] - M);
-            den += wq;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wq, v[q][e], acc[e]);
+        for (int e = 0; e < EPL; ++e) v[q][e] = 0.f;
+        if (k < it.count) {
+          w[q] = __ldcg(lse_h + (size_t)k * p.hq);
+          const float* src = o_h + (size_t)k * p.hq * D;
+          if constexpr (EPL == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+            v[q][0] = t.x, v[q][1] = t.y, v[q][2] = t.z, v[q][3] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+            v[q][0] = t.x, v[q][1] = t.y;
           }
         }
       }
+      float mr = w[0];
+#pragma unroll
+      for (int q = 1; q < G; ++q) mr = fmaxf(mr, w[q]);
+      const float m_new = fmaxf(M, mr);
+      if (m_new == -INFINITY) continue;  // nothing visible so far
+      const float sc = exp2f(M - m_new);  // 0 while M is still -inf
+      den *= sc;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] *= sc;
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        const float wq = exp2f(w[q] - m_new);  // 0 for absent or empty partials
+        den += wq;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wq, v[q][e], acc[e]);
+      }
+      M = m_new;
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     float* dst = p.out + ((size_t)it.tok * p.hq + h) * D + lane * EPL;
