@@ -120,12 +120,14 @@ struct Bars {
   __device__ uint32_t o_empty() const { return b + 8 * (4 * S + 11); }
 };
 
-// Bounded wait.  Returns false (and does not wait) once the CTA has aborted;
-// a wait that exceeds the limit aborts the CTA and records the error.
+// Bounded wait.  Returns false (without waiting further) once the CTA has
+// aborted; a wait that exceeds the limit aborts the CTA and records the
+// error.  A phase that has already completed returns true at once: every
+// issue after a wait checks the abort flag itself.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Shared& sh,
                                          int32_t* err, long long limit_ns) {
-  if (*sh.abort_flag) return false;
   if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (*sh.abort_flag) return false;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -219,7 +221,7 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
                            const Bars<D>& B, uint32_t tmem) {
   using C = Cfg<D>;
   uint32_t g = 0, gm = 0, nu = 0;
-  const uint32_t qbase = sh.base + C::kOffQ;
+  const uint64_t dq = ptx::sdesc_sw128(sh.base + C::kOffQ, 16, 1024);  // the query tile
   bool issued = false;
   UnitDesc un = u0 < u1 ? p.units[u0] : UnitDesc{};
   for (int ui = u0; ui < u1; ++ui) {
@@ -232,7 +234,6 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
     }
     const bool qok = wait_bar(B.q_full(0), nu & 1, sh, p.err, p.wait_timeout_ns);
     ptx::tc_fence_after();
-    const uint32_t qb = qbase;
     const uint32_t o_tmem = tmem + 128;
     auto issue_pv = [&](int jj) {
       const int pb = (gm + jj) & 1;  // P(jj) sits in the first 32 columns of S buffer pb
@@ -245,12 +246,13 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       ptx::tc_fence_after();
       const int nbk = min(kBpt, u.blk1 - (u.blk0 + kBpt * jj));
       if (ok && !*sh.abort_flag) {
-        const uint32_t vb = sh.base + C::kOffV + s * C::kTileBytes;
-        for (int kk = 0; kk < nbk; ++kk) {  // one page (16 tokens = 8 columns of P) per MMA
-          const uint64_t bd = ptx::sdesc_sw128(vb + kk * C::kBlockBytes, 2048, 1024);
-          ptx::mma_bf16_ts(o_tmem, tmem + pb * kTileTok + kk * 8, bd, C::kIdescPV,
-                           (jj > 0 || kk > 0) ? 1u : 0u);
-        }
+        // descriptors: the 14-bit start address field (16-byte units) of the
+        // stage's base descriptor plus the page offset (no carry: the shared
+        // window is below 256 KB)
+        const uint64_t dv = ptx::sdesc_sw128(sh.base + C::kOffV + s * C::kTileBytes, 2048, 1024);
+        for (int kk = 0; kk < nbk; ++kk)  // one page (16 tokens = 8 columns of P) per MMA
+          ptx::mma_bf16_ts(o_tmem, tmem + pb * kTileTok + kk * 8, dv + kk * (C::kBlockBytes >> 4),
+                           C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
         issued = true;
       }
       ptx::mma_commit(B.vempty(s));
@@ -264,13 +266,13 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       ok = ok && wait_bar(B.pv_done(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
       ptx::tc_fence_after();
       if (ok && !*sh.abort_flag) {
-        const uint32_t kb = sh.base + C::kOffK + s * C::kTileBytes;
+        const uint64_t dk = ptx::sdesc_sw128(sh.base + C::kOffK + s * C::kTileBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qoff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
           const uint32_t koff = (kk >> 2) * (kTileTok * 128) + (kk & 3) * 32;
-          ptx::mma_bf16(tmem + sb * kTileTok, ptx::sdesc_sw128(qb + qoff, 16, 1024),
-                        ptx::sdesc_sw128(kb + koff, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+          ptx::mma_bf16(tmem + sb * kTileTok, dq + (qoff >> 4), dk + (koff >> 4), C::kIdescQK,
+                        kk > 0 ? 1u : 0u);
         }
         issued = true;
       }
