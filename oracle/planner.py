@@ -250,12 +250,23 @@ def build_plan(parent, node_kv_len, node_page_offsets, node_pages, page_size,
         target = _ceil(work, o.split_waves * o.num_sms)
         chunk = max(_ceil(o.min_split_tokens, page_size), _ceil(target, bpt) * bpt)
     chunk = max(chunk, bpt)
+    # Thin tensor-core groups longer than a packable group (more than 8
+    # pages) run packed by kv head: a unit covers four kv heads, so the
+    # automatic split gives them a quarter of the chunk (not below the
+    # minimum split).
+    def head_thin(g):
+        return (not o.no_pack and g["path"] == "mma" and g["qtiles"] == 1
+                and g["rows"] <= 32 and 32 % r == 0 and n_kv_heads % 4 == 0
+                and len(g["blocks"]) > 8)
     for g in groups:
         nb = len(g["blocks"])
-        if nb <= chunk:
+        cg = chunk
+        if o.split_tokens == 0 and head_thin(g):
+            cg = max(_ceil(o.min_split_tokens, page_size), _ceil(chunk, 4))
+        if nb <= cg:
             g["chunks"] = [[0, nb]]
         else:
-            k = _ceil(nb, chunk)
+            k = _ceil(nb, cg)
             cb = _ceil(_ceil(nb, k), bpt) * bpt
             g["chunks"] = [[s, min(nb, s + cb)] for s in range(0, nb, cb)]
     # Partial results per query token: one per (group on its path, chunk).
@@ -276,9 +287,18 @@ def build_plan(parent, node_kv_len, node_page_offsets, node_pages, page_size,
         if g["path"] == "mma" and g["rows"] <= 32 and 32 % r == 0:
             return "mma"
         return None  # CUDA-core groups are not packed
+    # The longer thin tensor-core groups share units by kv head instead:
+    # four kv heads of the group per unit, one unit per chunk and group of
+    # four kv heads.
     kinds = [packable(g) for g in groups]
-    n_units = sum(n_kv_heads * g["qtiles"] * len(g["chunks"])
-                  for g, k in zip(groups, kinds) if k is None)
+    n_units = 0
+    for g, k in zip(groups, kinds):
+        if k is not None:
+            continue
+        if head_thin(g):
+            n_units += len(g["chunks"]) * (n_kv_heads // 4)
+        else:
+            n_units += n_kv_heads * g["qtiles"] * len(g["chunks"])
     for kind in ("mma", "simt"):
         n_units += n_kv_heads * _ceil(sum(1 for k in kinds if k == kind), 4)
     return {

@@ -301,14 +301,24 @@ tree_attn_status build_host_plan(
   }
   chunk = std::max<int64_t>(chunk, kBlocksPerTile);
   p.chunk_blocks = chunk;
+  // Thin tensor-core groups longer than a packable group run packed by kv
+  // head (see the units below): a unit covers four kv heads, so the
+  // automatic split gives them a quarter of the chunk, not below the minimum.
+  auto head_thin = [&](const GroupInfo& g) {
+    return !opt.no_pack && g.path == kPathMma && g.qtiles == 1 && g.rows <= kPackMmaRows &&
+           kPackMmaRows % r == 0 && hkv % kPackSlots == 0 && g.nblk > kPackMaxBlocks;
+  };
   for (auto& g : p.groups) {
     g.chunk_off = (int32_t)p.chunk_lo.size();
     int64_t nb = g.nblk;
-    if (nb <= chunk) {
+    int64_t cg = chunk;
+    if (opt.split_tokens == 0 && head_thin(g))
+      cg = std::max(ceil_div(opt.min_split_tokens, page_size), ceil_div(chunk, (int64_t)kPackSlots));
+    if (nb <= cg) {
       p.chunk_lo.push_back(0);
       p.chunk_hi.push_back((int32_t)nb);
     } else {
-      int64_t k = ceil_div(nb, chunk);
+      int64_t k = ceil_div(nb, cg);
       int64_t cb = ceil_div(ceil_div(nb, k), kBlocksPerTile) * kBlocksPerTile;
       for (int64_t s = 0; s < nb; s += cb) {
         p.chunk_lo.push_back((int32_t)s);
@@ -359,8 +369,11 @@ tree_attn_status build_host_plan(
     if (k == kPathMma) pack_mma.push_back((int32_t)gi);
     if (k == kPathSimt) pack_simt.push_back((int32_t)gi);
   }
+  // Longer thin tensor-core groups are packed by kv head: four kv heads of
+  // the group share a unit, slot k holding kv head kvh + k, and KV tile j
+  // holds page j of the chunk once per slot.
   for (auto& g : p.groups) {
-    if (packable(g) >= 0) continue;
+    if (packable(g) >= 0 || head_thin(g)) continue;
     const int tile = g.path == kPathMma ? kMmaTileRows : kSimtTileRows;
     for (int kvh = 0; kvh < hkv; ++kvh)
       for (int c = 0; c < g.nchunks; ++c)
@@ -434,6 +447,46 @@ tree_attn_status build_host_plan(
   };
   emit_packs(pack_mma, kPathMma);
   emit_packs(pack_simt, kPathSimt);
+  for (size_t gi = 0; gi < p.groups.size(); ++gi) {
+    const GroupInfo& g = p.groups[gi];
+    if (!head_thin(g)) continue;
+    // row records slot by slot: the group's tokens once per slot
+    const int32_t tok_off = (int32_t)p.gtok.size();
+    for (int k = 0; k < kPackSlots; ++k)
+      for (int e = 0; e < kPackMmaRows / r; ++e) {
+        if (e < g.ntok) {
+          p.gtok.push_back(p.gtok[g.tok_off + e]);
+          p.gvis.push_back(p.gvis[g.tok_off + e]);
+          p.gpbase.push_back(p.gpbase[g.tok_off + e]);
+        } else {
+          p.gtok.push_back(-1);
+          p.gvis.push_back(0);
+          p.gpbase.push_back(-1);
+        }
+        p.gslot.push_back(k);
+      }
+    for (int c = 0; c < g.nchunks; ++c) {
+      const int32_t blk0 = (int32_t)p.blk_page.size();
+      for (int32_t b = p.chunk_lo[g.chunk_off + c]; b < p.chunk_hi[g.chunk_off + c]; ++b)
+        for (int k = 0; k < kPackSlots; ++k) {
+          p.blk_page.push_back(p.blk_page[g.blk_off + b]);
+          p.blk_meta.push_back(p.blk_meta[g.blk_off + b]);
+        }
+      const int32_t blk1 = (int32_t)p.blk_page.size();
+      for (int kvh = 0; kvh < hkv; kvh += kPackSlots) {
+        UnitDesc u;
+        u.tok_off = tok_off;
+        u.kvh = kvh;
+        u.row0 = 0;
+        u.nrows = kPackSlots * kPackMmaRows;
+        u.blk0 = blk0;
+        u.blk1 = blk1;
+        u.chunk = c;
+        u.path = kPathMma | kUnitHeads;
+        p.units.push_back(u);
+      }
+    }
+  }
   const int64_t nu = (int64_t)p.units.size();
   p.grid = (int32_t)std::min<int64_t>(nu, (int64_t)std::max(1, opt.num_sms) * kCtasPerSm);
   {
@@ -441,7 +494,7 @@ tree_attn_status build_host_plan(
     for (int64_t i = 0; i < nu; ++i) order[i] = (int32_t)i;
     // blocks streamed plus a fixed start-up and epilogue cost per unit
     auto cost = [&](int32_t i) {
-      return (int64_t)(p.units[i].blk1 - p.units[i].blk0) + (p.units[i].path == kPathMma ? 6 : 3);
+      return (int64_t)(p.units[i].blk1 - p.units[i].blk0) + ((p.units[i].path & kPathMma) ? 6 : 3);
     };
     std::stable_sort(order.begin(), order.end(),
                      [&](int32_t a, int32_t b) { return cost(a) > cost(b); });

@@ -33,6 +33,7 @@ constexpr int kPackSimtRows = 2;    // rows per slot on CUDA cores
 static_assert(kPackSlots == kBlocksPerTile, "one page per slot per tile");
 constexpr int kPathSimt = 0;
 constexpr int kPathMma = 1;
+constexpr int kUnitHeads = 2;  // with kPathMma: slot k of the unit is kv head kvh + k
 
 struct Options {
   int64_t gamma = 64;
@@ -62,7 +63,7 @@ struct UnitDesc {
   int32_t blk0;     // first block (absolute index into the block list)
   int32_t blk1;     // one past the last block
   int32_t chunk;    // chunk index inside the group (selects the partial slot)
-  int32_t path;     // kPathSimt or kPathMma
+  int32_t path;     // kPathSimt, kPathMma, or kPathMma | kUnitHeads
 };
 
 struct GroupInfo {

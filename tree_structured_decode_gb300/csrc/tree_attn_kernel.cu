@@ -185,6 +185,7 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
         continue;
       if (*sh.abort_flag) continue;
       ptx::mbar_arrive_expect_tx(full, (uint32_t)nb * C::kBlockBytes);
+      const int kvh = u.kvh, hstep = (u.path & kUnitHeads) ? 1 : 0;  // page bb's kv head
       const uint32_t dst = sh.base + (kIsV ? C::kOffV : C::kOffK) + s * C::kTileBytes;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
@@ -192,12 +193,12 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
           if constexpr (!kIsV) {
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h)
-              ptx::tma_load_4d(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0, u.kvh, page[bb],
-                               full);
+              ptx::tma_load_4d(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0, kvh + bb * hstep,
+                               page[bb], full);
           } else if constexpr (D == 128) {  // both 64-column halves of V in one box
-            ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, u.kvh, page[bb], full);
+            ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, kvh + bb * hstep, page[bb], full);
           } else {
-            ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, u.kvh, page[bb], full);
+            ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, kvh + bb * hstep, page[bb], full);
           }
         }
       }
@@ -228,7 +229,7 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
     const UnitDesc u = un;
     if (ui + 1 < u1) un = p.units[ui + 1];
     const int T = unit_tiles(u);
-    if (u.path != kPathMma || T == 0) {
+    if (!(u.path & kPathMma) || T == 0) {
       g += T;
       continue;
     }
@@ -619,9 +620,15 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
 __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1) {
   for (; k < u1; ++k) {
     const UnitDesc u = p.units[k];
-    if (u.path == kPathMma && u.blk1 > u.blk0) return k;
+    if ((u.path & kPathMma) && u.blk1 > u.blk0) return k;
   }
   return -1;
+}
+
+// q head of row `row` (= row0 + tile row) of a unit; in a unit packed by kv
+// head, 32-row slot k belongs to kv head kvh + k.
+__device__ __forceinline__ int unit_head(const AttnParams& p, const UnitDesc& u, int row) {
+  return (u.kvh + ((u.path & kUnitHeads) ? row / kPackMmaRows : 0)) * p.gqa + row % p.gqa;
 }
 
 // Row tid of unit k's query tile: its record (token, visible end, partial
@@ -638,7 +645,7 @@ __device__ __forceinline__ QRow q_row(const AttnParams& p, int k, int tid) {
   QRow r{GroupTok{-1, 0, -1, 0}, p.q};
   if (tid < u.nrows) r.gt = p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa];
   if (r.gt.tok >= 0) {
-    const int h = u.kvh * p.gqa + (u.row0 + tid) % p.gqa;
+    const int h = unit_head(p, u, u.row0 + tid);
     r.src = p.q + ((size_t)r.gt.tok * p.hq + h) * D;
   }
   return r;
@@ -661,7 +668,7 @@ template <int D, int N>
 __device__ __forceinline__ void write_row_cols(const AttnParams& p, const UnitDesc& u, int grow,
                                                const GroupTok& gt, const float* o, int c0, float inv,
                                                float lse2, bool with_lse) {
-  const int h = u.kvh * p.gqa + grow % p.gqa;
+  const int h = unit_head(p, u, grow);
   float* dst;
   if (gt.pbase < 0) {
     dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
@@ -710,7 +717,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
                                         : GroupTok{-1, 0, -1, 0};
       if (gt.tok >= 0 && !*sh.abort_flag) {
         const int grow = u.row0 + tid;
-        const int h = u.kvh * p.gqa + grow % p.gqa;
+        const int h = unit_head(p, u, grow);
         float* dst;
         if (gt.pbase < 0) {
           dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
@@ -726,7 +733,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       }
       continue;
     }
-    if (u.path != kPathMma) {
+    if (!(u.path & kPathMma)) {
       simt_unit<D>(p, u, g, T, sh, B);
       g += T;
       continue;
@@ -952,7 +959,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     ptx::tc_fence_before();
     ptx::mbar_arrive(B.o_empty());  // O is free before the (rare, slow) merge
     if (ok && row_ok && gt_row.pbase >= 0 && p.merge_fused && !*sh.abort_flag)
-      merge_row_thread<D>(p, gt_row, u.kvh * p.gqa + (u.row0 + tid) % p.gqa);
+      merge_row_thread<D>(p, gt_row, unit_head(p, u, u.row0 + tid));
     g += T;
     gm += T;
     ++nu;
