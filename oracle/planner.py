@@ -45,7 +45,7 @@ class PlannerOptions:
     kv_tile_tokens: int = 64             # chunk granularity (tokens)
     split_tokens: int = 0                # 0 = automatic split, < 0 = never
     min_split_tokens: int = 256          # smallest automatic chunk
-    split_waves: int = 4                 # automatic split aims at waves x SMs
+    split_waves: int = 2                 # automatic split aims at waves x SMs
     num_sms: int = 152                   # SM count the split targets
     force_path: int = 0                  # 0 by rows, 1 CUDA cores, 2 MMA
     no_pack: int = 0                     # 1: never pack thin groups

@@ -43,7 +43,7 @@ struct Options {
   int32_t mma_min_rows = 1;
   int32_t split_tokens = 0;
   int32_t min_split_tokens = 256;
-  int32_t split_waves = 4;
+  int32_t split_waves = 2;
   int32_t num_sms = 152;
   int32_t force_path = 0;
   int32_t host_only = 0;
