@@ -160,3 +160,26 @@ def test_packed_thin_groups(hq, hkv, path):
         out, lse, _ = run_gpu(spec, q, k, v, **opts)
         ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
         compare(out, lse, ref, ref_lse)
+
+
+# ----------------------------------------------------------------- kv-head packed units
+@pytest.mark.parametrize("hq,hkv,ntok", [(16, 4, 1), (8, 4, 2), (32, 8, 6), (64, 8, 2)])
+def test_kv_head_packed_units(hq, hkv, ntok):
+    # leaves longer than 8 pages with a few (causal, speculative) query tokens
+    # each, under a long root: groups of <= 32 rows per kv head run four kv
+    # heads to a unit
+    rng = np.random.default_rng(hq * 31 + ntok)
+    nleaf = 6
+    lens = [600] + [int(x) for x in rng.integers(140, 420, size=nleaf)]
+    parent = [-1] + [0] * nleaf
+    qnode = [v for v in range(1, nleaf + 1) for _ in range(ntok)]
+    qend = [lens[v] - (ntok - 1 - j) for v in range(1, nleaf + 1) for j in range(ntok)]
+    spec = W._finish("heads", parent, lens, qnode, qend, hq, hkv, 128, seed=11)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    units = {}
+    for name, opts in (("auto", {}), ("split", {"split_tokens": 128}), ("unpacked", {"no_pack": 1})):
+        out, lse, stats = run_gpu(spec, q, k, v, **opts)
+        compare(out, lse, ref, ref_lse)
+        units[name] = stats["n_units"]
+    assert units["auto"] < units["unpacked"]  # the leaves were packed

@@ -105,3 +105,18 @@ def test_planning_is_fast_on_the_irregular_tree():
     spec = W.config_irregular()
     _, stats = _native(spec)
     assert stats["plan_ms"] < 200.0
+
+
+@pytest.mark.parametrize("hq,hkv,ntok", [(16, 4, 1), (8, 4, 2), (32, 8, 6), (64, 4, 3), (16, 2, 2),
+                                         (64, 8, 1)])
+def test_kv_head_packing_matches_reference(hq, hkv, ntok):
+    # long thin leaves: groups of <= 32 rows per kv head pack four kv heads to
+    # a unit with a quarter of the automatic chunk (hkv a multiple of 4);
+    # others stay one unit per kv head
+    rng = np.random.default_rng(hq * 31 + ntok)
+    lens = [600] + [int(x) for x in rng.integers(140, 900, size=6)]
+    qnode = [v for v in range(1, 7) for _ in range(ntok)]
+    qend = [lens[v] - (ntok - 1 - j) for v in range(1, 7) for j in range(ntok)]
+    spec = W._finish("heads", [-1] + [0] * 6, lens, qnode, qend, hq, hkv, 128, seed=11)
+    for opt in ({}, {"split_tokens": 128}, {"no_pack": 1}, {"num_sms": 8}):
+        _same(spec, **opt)
