@@ -66,7 +66,7 @@ def test_static_entry_point_refuses_a_plan_larger_than_its_scratch():
     import tree_structured_decode_gb300 as ta
     from tree_structured_decode_gb300 import _abi
 
-    spec = W.config_irregular()  # ~0.27 GB of partial results: far above the scratch
+    spec = W.config_irregular()  # ~0.14 GB of partial results: far above the scratch
     q = torch.zeros((spec.n_queries, spec.n_q_heads, spec.head_dim), dtype=torch.bfloat16,
                     device="cuda")
     kv = torch.zeros((1,), dtype=torch.bfloat16, device="cuda")

@@ -1,6 +1,7 @@
 // Log-sum-exp merge kernel (sm_103a).
 //
-// merge pass: per (query token, q head), fold its partials:
+// merge pass: per (query token, q head), fold its partials (O in fp16,
+// lse in fp32):
 //   m = max lse_i, w_i = 2^(lse_i - m), O = sum w_i O_i / sum w_i,
 //   lse = m + log2 sum w_i   (partials keep lse in base 2).
 #include <cuda_runtime.h>
@@ -8,20 +9,22 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace ta {
 namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// One warp per (merge token, q head).  The partials are read eight at a time
+// One warp per (merge token, q head).  The partials are read G at a time
 // (lse and the lane's columns of every O row in flight together) and folded
 // online: the running max M only grows, and the sums kept so far are scaled
-// by 2^(M_old - M_new) when it does.
-template <int D>
-__global__ void __launch_bounds__(256, 4) lse_merge_kernel(const MergeParams p) {
+// by 2^(M_old - M_new) when it does.  G = 8 keeps the registers low for
+// many short merges; plans whose tokens have more partials use G = 24 so a
+// token takes one round of loads.
+template <int D, int G, int kMinBlocks>
+__global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeParams p) {
   constexpr int EPL = D / 32;  // 4 or 2 columns per lane
-  constexpr int G = 8;         // partials per round
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -30,7 +33,7 @@ __global__ void __launch_bounds__(256, 4) lse_merge_kernel(const MergeParams p) 
     const MergeItem it = p.items[idx / p.hq];
     const int h = idx % p.hq;
     const float* lse_h = p.part_lse + (size_t)it.poff * p.hq + h;  // partial k at lse_h[k * hq]
-    const float* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + lane * EPL;
+    const uint16_t* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + lane * EPL;  // fp16
     float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
@@ -44,13 +47,14 @@ __global__ void __launch_bounds__(256, 4) lse_merge_kernel(const MergeParams p) 
         for (int e = 0; e < EPL; ++e) v[q][e] = 0.f;
         if (k < it.count) {
           w[q] = __ldcg(lse_h + (size_t)k * p.hq);
-          const float* src = o_h + (size_t)k * p.hq * D;
+          const uint16_t* src = o_h + (size_t)k * p.hq * D;
           if constexpr (EPL == 4) {
-            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-            v[q][0] = t.x, v[q][1] = t.y, v[q][2] = t.z, v[q][3] = t.w;
+            const uint2 t = __ldcg(reinterpret_cast<const uint2*>(src));
+            const float2 a = ptx::unpack_f16(t.x), b = ptx::unpack_f16(t.y);
+            v[q][0] = a.x, v[q][1] = a.y, v[q][2] = b.x, v[q][3] = b.y;
           } else {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-            v[q][0] = t.x, v[q][1] = t.y;
+            const float2 a = ptx::unpack_f16(__ldcg(reinterpret_cast<const unsigned int*>(src)));
+            v[q][0] = a.x, v[q][1] = a.y;
           }
         }
       }
@@ -89,10 +93,18 @@ cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
   const long long warps = (long long)p.n_items * p.hq;
   const int blocks = (int)((warps + 7) / 8 < 152 * 16 ? (warps + 7) / 8 : 152 * 16);
-  if (d == 128)
-    lse_merge_kernel<128><<<blocks, 256, 0, s>>>(p);
-  else
-    lse_merge_kernel<64><<<blocks, 256, 0, s>>>(p);
+  const bool wide_rounds = p.max_count > 8;  // tokens with up to 24 partials: one round
+  if (d == 128) {
+    if (wide_rounds)
+      lse_merge_kernel<128, 24, 1><<<blocks, 256, 0, s>>>(p);
+    else
+      lse_merge_kernel<128, 8, 4><<<blocks, 256, 0, s>>>(p);
+  } else {
+    if (wide_rounds)
+      lse_merge_kernel<64, 24, 1><<<blocks, 256, 0, s>>>(p);
+    else
+      lse_merge_kernel<64, 8, 4><<<blocks, 256, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -37,7 +37,7 @@ struct AttnParams {
   const uint16_t* v;
   float* out;                // [nq][hq][d]
   float* lse;                // [nq][hq] natural log, or null
-  float* part_o;             // [n_partials][hq][d]
+  uint16_t* part_o;          // [n_partials][hq][d] fp16 bits (normalised partial O)
   float* part_lse;           // [n_partials][hq], log2 units
   int32_t* err;              // device error word
   int32_t hq, hkv, gqa, n_units;
@@ -55,7 +55,8 @@ struct AttnParams {
 struct MergeParams {
   const MergeItem* items;
   int32_t n_items, hq;
-  const float* part_o;
+  int32_t max_count;         // most partials of any merged token
+  const uint16_t* part_o;    // fp16 bits
   const float* part_lse;
   float* out;
   float* lse;

@@ -23,7 +23,7 @@ struct tree_attn_plan_s {
   const int32_t* d_cta_off = nullptr;
   const ta::MergeItem* d_merge = nullptr;
   int32_t* d_err = nullptr;
-  float* d_part_o = nullptr;
+  uint16_t* d_part_o = nullptr;  // fp16
   float* d_part_lse = nullptr;
   int32_t* d_merge_cnt = nullptr;
   size_t merge_cnt_bytes = 0;

@@ -1,6 +1,8 @@
 // C ABI of libtreeattn: plan construction, device upload, launches, status.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include <chrono>
 #include <cmath>
 #include <cstdlib>
@@ -106,7 +108,7 @@ tree_attn_status upload(tree_attn_plan_s* P) {
   P->d_tok_poff = reinterpret_cast<const int32_t*>(b + secs[6].off);
 
   const size_t np = (size_t)h.n_partials * h.hq;
-  const size_t o_bytes = align_up(np * h.d * sizeof(float), 256);
+  const size_t o_bytes = align_up(np * h.d * sizeof(uint16_t), 256);  // fp16 partial O
   const size_t l_bytes = align_up(np * sizeof(float), 256);
   const size_t c_bytes = h.n_partials ? align_up((size_t)h.nq * h.hq * sizeof(int32_t), 256) : 0;
   P->work_bytes = o_bytes + l_bytes + c_bytes;
@@ -116,7 +118,7 @@ tree_attn_status upload(tree_attn_plan_s* P) {
       P->dwork = nullptr;
       return set_err(TA_ERR_OOM, std::string("cudaMalloc(workspace): ") + cudaGetErrorString(e));
     }
-    P->d_part_o = static_cast<float*>(P->dwork);
+    P->d_part_o = static_cast<uint16_t*>(P->dwork);
     P->d_part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(P->dwork) + o_bytes);
     if (c_bytes) {
       P->d_merge_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(P->dwork) + o_bytes + l_bytes);
@@ -278,6 +280,7 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
     mp.items = P->d_merge;
     mp.n_items = (int32_t)h.merge_tok.size();
     mp.hq = h.hq;
+    mp.max_count = h.pcount.empty() ? 0 : *std::max_element(h.pcount.begin(), h.pcount.end());
     mp.part_o = P->d_part_o;
     mp.part_lse = P->d_part_lse;
     mp.out = out;

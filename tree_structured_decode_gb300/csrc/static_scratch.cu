@@ -114,7 +114,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   const size_t o_mtok = take(nmerge * 4), o_poff = take(nq * 4), o_pcnt = take(nq * 4);
   const size_t o_merge = take(nmerge * sizeof(MergeItem));
   const size_t o_err = take(16 * sizeof(int32_t));
-  const size_t o_po = take(np * (size_t)h.d * sizeof(float));
+  const size_t o_po = take(np * (size_t)h.d * sizeof(uint16_t));  // fp16 partial O
   const size_t o_pl = take(np * sizeof(float));
   const size_t ncnt = h.n_partials ? nq * (size_t)h.hq : 0;
   const size_t o_cnt = take(ncnt * sizeof(int32_t));
@@ -184,7 +184,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   ap.v = static_cast<const uint16_t*>(v_pages);
   ap.out = out;
   ap.lse = lse;
-  ap.part_o = reinterpret_cast<float*>(base + o_po);
+  ap.part_o = reinterpret_cast<uint16_t*>(base + o_po);
   ap.part_lse = reinterpret_cast<float*>(base + o_pl);
   ap.err = reinterpret_cast<int32_t*>(base + o_err);
   ap.hq = h.hq;
@@ -204,6 +204,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
     mp.items = reinterpret_cast<const MergeItem*>(base + o_merge);
     mp.n_items = (int32_t)nmerge;
     mp.hq = h.hq;
+    mp.max_count = h.pcount.empty() ? 0 : *std::max_element(h.pcount.begin(), h.pcount.end());
     mp.part_o = ap.part_o;
     mp.part_lse = ap.part_lse;
     mp.out = out;

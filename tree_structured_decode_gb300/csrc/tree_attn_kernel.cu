@@ -336,14 +336,20 @@ __device__ void merge_row_thread(const AttnParams& p, const GroupTok& gt, int h)
       for (int k = 0; k < gt.pcount(); ++k) {
         const size_t slot = (size_t)(poff + k) * p.hq + h;
         const float w = ptx::ex2(__ldcg(p.part_lse + slot) - m);
-        const float4* src = reinterpret_cast<const float4*>(p.part_o + slot * D + c0);
+        const uint4* src = reinterpret_cast<const uint4*>(p.part_o + slot * D + c0);  // fp16
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 v = __ldcg(src + e);
-          acc[e].x = fmaf(w, v.x, acc[e].x);
-          acc[e].y = fmaf(w, v.y, acc[e].y);
-          acc[e].z = fmaf(w, v.z, acc[e].z);
-          acc[e].w = fmaf(w, v.w, acc[e].w);
+        for (int e = 0; e < 4; ++e) {
+          const uint4 v = __ldcg(src + e);
+          const float2 a = ptx::unpack_f16(v.x), b = ptx::unpack_f16(v.y);
+          const float2 c = ptx::unpack_f16(v.z), dd = ptx::unpack_f16(v.w);
+          acc[2 * e].x = fmaf(w, a.x, acc[2 * e].x);
+          acc[2 * e].y = fmaf(w, a.y, acc[2 * e].y);
+          acc[2 * e].z = fmaf(w, b.x, acc[2 * e].z);
+          acc[2 * e].w = fmaf(w, b.y, acc[2 * e].w);
+          acc[2 * e + 1].x = fmaf(w, c.x, acc[2 * e + 1].x);
+          acc[2 * e + 1].y = fmaf(w, c.y, acc[2 * e + 1].y);
+          acc[2 * e + 1].z = fmaf(w, dd.x, acc[2 * e + 1].z);
+          acc[2 * e + 1].w = fmaf(w, dd.y, acc[2 * e + 1].w);
         }
       }
 #pragma unroll
@@ -380,8 +386,13 @@ __device__ void merge_row_warp(const AttnParams& p, const GroupTok& gt, int h, i
       const size_t slot = (size_t)(poff + k) * p.hq + h;
       const float w = ptx::ex2(__ldcg(p.part_lse + slot) - m);
       den += w;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(p.part_o + slot * D + lane * EPL);
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, __ldcg(p.part_o + slot * D + lane * EPL + e), acc[e]);
+      for (int e = 0; e < EPL; e += 2) {
+        const float2 v = ptx::unpack_f16(__ldcg(src + e / 2));
+        acc[e] = fmaf(w, v.x, acc[e]);
+        acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+      }
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -599,17 +610,18 @@ __device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, in
       const int h = u.kvh * p.gqa + grow % p.gqa;
       const float inv = L > 0.f ? 1.f / L : 0.f;
       const float lse2 = L > 0.f ? M + __log2f(L) : -INFINITY;
-      float* dst;
       if (gt.pbase < 0) {
-        dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
+        float* dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
         if (lane == 0 && p.lse) p.lse[(size_t)gt.tok * p.hq + h] = lse2 * kLn2;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = O[e] * inv;
       } else {
         const size_t ps = (size_t)(gt.pbase + u.chunk) * p.hq + h;
-        dst = p.part_o + ps * D;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.part_o + ps * D + lane * EPL);
         if (lane == 0) p.part_lse[ps] = lse2;
-      }
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = O[e] * inv;
+        for (int e = 0; e < EPL; e += 2) dst[e / 2] = ptx::pack_f16(O[e] * inv, O[e + 1] * inv);
+      }
       if (gt.pbase >= 0 && p.merge_fused) merge_row_warp<D>(p, gt, h, lane);
     }
   }
@@ -663,25 +675,29 @@ __device__ __forceinline__ void load_q(const QRow& r, uint32_t qb, int tid) {
 }
 
 // Write columns [c0, c0 + N) of row `grow`'s result (normalised O, and lse
-// when with_lse) to the output or to its partial slot.
+// when with_lse) to the output (fp32) or to its partial slot (fp16).
 template <int D, int N>
 __device__ __forceinline__ void write_row_cols(const AttnParams& p, const UnitDesc& u, int grow,
                                                const GroupTok& gt, const float* o, int c0, float inv,
                                                float lse2, bool with_lse) {
   const int h = unit_head(p, u, grow);
-  float* dst;
   if (gt.pbase < 0) {
-    dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
+    float* dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
     if (with_lse && p.lse) p.lse[(size_t)gt.tok * p.hq + h] = lse2 * kLn2;
+#pragma unroll
+    for (int c = 0; c < N; c += 4)
+      *reinterpret_cast<float4*>(dst + c0 + c) =
+          make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
   } else {
     const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
-    dst = p.part_o + slot * D;
+    uint16_t* dst = p.part_o + slot * D;
     if (with_lse) p.part_lse[slot] = lse2;
-  }
 #pragma unroll
-  for (int c = 0; c < N; c += 4)
-    *reinterpret_cast<float4*>(dst + c0 + c) =
-        make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+    for (int c = 0; c < N; c += 8)
+      *reinterpret_cast<uint4*>(dst + c0 + c) =
+          make_uint4(ptx::pack_f16(o[c] * inv, o[c + 1] * inv), ptx::pack_f16(o[c + 2] * inv, o[c + 3] * inv),
+                     ptx::pack_f16(o[c + 4] * inv, o[c + 5] * inv), ptx::pack_f16(o[c + 6] * inv, o[c + 7] * inv));
+  }
 }
 
 // The four compute warps: thread i owns TMEM lane / query row i.
@@ -718,17 +734,17 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       if (gt.tok >= 0 && !*sh.abort_flag) {
         const int grow = u.row0 + tid;
         const int h = unit_head(p, u, grow);
-        float* dst;
         if (gt.pbase < 0) {
-          dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
+          float* dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
           if (p.lse) p.lse[(size_t)gt.tok * p.hq + h] = -INFINITY;
+          for (int c = 0; c < D; c += 4)
+            *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
           const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
-          dst = p.part_o + slot * D;
+          uint16_t* dst = p.part_o + slot * D;
           p.part_lse[slot] = -INFINITY;
+          for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
         }
-        for (int c = 0; c < D; c += 4)
-          *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
         if (gt.pbase >= 0 && p.merge_fused) merge_row_thread<D>(p, gt, h);
       }
       continue;
