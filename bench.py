@@ -160,6 +160,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max_over_ranks(vals, world, device):
+    """Each timing's maximum over all ranks: the slowest replica sets the
+    step time of the whole job."""
+    if world <= 1:
+        return [float(x) for x in vals]
+    import torch
+
+    t = torch.tensor([float(x) for x in vals], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def aggregate_gbs(bytes_per_step, world, step_ms):
+    """Whole-job throughput: every replica processes one step's bytes in the
+    (slowest) step time."""
+    return bytes_per_step * world / (step_ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------------------- ours
 def bench_ours(args, rank, world, local):
     import torch
@@ -245,12 +263,9 @@ def bench_ours(args, rank, world, local):
     t_step = float(np.mean(step_ms))
     t_part = float(np.mean(part_ms))
     t_e2e = float(np.mean(e2e_ms))
-    if world > 1:
-        tt = torch.tensor([t_step, t_e2e, t_part], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_step, t_e2e, t_part = (float(x) for x in tt.tolist())
+    t_step, t_e2e, t_part = reduce_max_over_ranks([t_step, t_e2e, t_part], world, dev)
     hbm_peak, tc_peak, peak_kind = measured_peaks()
-    gbs = work["bytes"] * world / (t_step * 1e-3) / 1e9
+    gbs = aggregate_gbs(work["bytes"], world, t_step)
     kern_gbs = work["bytes"] / (t_part * 1e-3) / 1e9
     t_hbm = work["bytes"] / (hbm_peak * 1e9)
     t_tc = work["flops"] / (tc_peak * 1e12)
@@ -283,7 +298,7 @@ def bench_ours(args, rank, world, local):
                    "plan": {k: stats[k] for k in ("n_groups", "n_groups_mma", "n_units", "grid",
                                                   "n_partials", "chunk_tokens", "plan_ms")},
                    "plan_options": args.plan_opts},
-        "e2e": {"value": round(work["bytes"] * world / (t_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(aggregate_gbs(work["bytes"], world, t_e2e), 2), "unit": "GB/s",
                 "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
