@@ -183,3 +183,27 @@ def test_kv_head_packed_units(hq, hkv, ntok):
         compare(out, lse, ref, ref_lse)
         units[name] = stats["n_units"]
     assert units["auto"] < units["unpacked"]  # the leaves were packed
+
+
+# ----------------------------------------------------------------- extremes
+def test_largest_gqa_ratio():
+    # 128 q heads per kv head: one query token fills a 128-row tile, a few
+    # tokens make several query tiles of one group
+    spec = W._finish("gqa128", [-1, 0, 0], [300, 90, 33], [1, 1, 2, 2, 2], [90, 89, 33, 32, 31],
+                     128, 1, 64, seed=21)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    for opts in ({}, {"split_tokens": 64}):
+        out, lse, _ = run_gpu(spec, q, k, v, **opts)
+        ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+        compare(out, lse, ref, ref_lse)
+
+
+def test_tokens_with_more_partials_than_one_merge_round():
+    # a 2000-token root split into 64-token chunks: every token folds 32 or
+    # more partials (two rounds of the wide merge)
+    spec = W.two_level(2000, 3, 50, 8, 2, 128, seed=9)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, stats = run_gpu(spec, q, k, v, split_tokens=64)
+    assert stats["n_partials"] >= 32 * spec.n_queries
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    compare(out, lse, ref, ref_lse)
