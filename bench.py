@@ -190,7 +190,10 @@ def bench_ours(args, rank, world, local):
     work = algorithmic_work(spec)
     q, k, v = W.make_tensors(spec, device=dev)
     torch.cuda.synchronize()
-    plan = ta.Plan.from_spec(spec, **args.plan_opts)
+    opts = dict(args.plan_opts)
+    if args.edges != "greedy":  # plan ablation: every edge 0 (no joins) or 1 (join every chain)
+        opts["force_edges"] = np.full(spec.n_nodes, 1 if args.edges == "one" else 0, dtype=np.int8)
+    plan = ta.Plan.from_spec(spec, **opts)
     stats = plan.stats()
     out = torch.empty((spec.n_queries, spec.n_q_heads, spec.head_dim), dtype=torch.float32,
                       device=dev)
@@ -289,6 +292,7 @@ def bench_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step, 5),
+        "ms_per_step_p10_p50_p90": [round(float(x), 5) for x in np.percentile(step_ms, [10, 50, 90])],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, shuffled 16-token pages)",
         "config": {"workload": WORKLOAD_DESC[args.workload], "name": args.workload,
@@ -297,7 +301,7 @@ def bench_ours(args, rank, world, local):
                    "alg_bytes_per_step": work["bytes"], "alg_flops_per_step": work["flops"],
                    "plan": {k: stats[k] for k in ("n_groups", "n_groups_mma", "n_units", "grid",
                                                   "n_partials", "chunk_tokens", "plan_ms")},
-                   "plan_options": args.plan_opts},
+                   "plan_options": args.plan_opts, "edges": args.edges},
         "e2e": {"value": round(aggregate_gbs(work["bytes"], world, t_e2e), 2), "unit": "GB/s",
                 "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -391,6 +395,8 @@ def main():
     ap.add_argument("--workload", default="long", choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--edges", default="greedy", choices=["greedy", "zero", "one"],
+                    help="edge assignment: the greedy algorithm, or every edge 0 / 1 (ablation)")
     ap.add_argument("--plan", action="append", default=[], metavar="KEY=VALUE",
                     help="planner option (tree_attn_options field), e.g. --plan gamma=16")
     args = ap.parse_args()
