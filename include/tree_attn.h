@@ -174,6 +174,27 @@ tree_attn_status tree_attn_run(tree_attn_plan_t plan, const void* q,
                                const void* k_pages, const void* v_pages,
                                float* out, float* lse, void* stream);
 
+/* The step before the attention of a decode step: write the key and value
+ * of every query token into its own position of the paged cache.  A decode
+ * step appends the new tokens' K/V to their leaves before attending, so a
+ * node's length counts its query tokens (DeFT notes page, "Tree attention
+ * definition": the query's own token is the last one it sees); the TGI
+ * FlashDecoding pull request gives every query token its own KV slot.
+ * Token t of node u with visible end e (query_kv_end[t], or len_u) owns
+ * position e - 1 of u: page node_pages[off[u] + (e - 1) / 16], slot
+ * (e - 1) % 16; tokens with e = 0 own none and are skipped.
+ *   k_new, v_new      device bf16 [n_query_tokens][n_kv_heads][head_dim]: the
+ *                     tokens' keys and values (16-byte aligned), read.
+ *   k_pages, v_pages  the page pools of tree_attn_run(); only the tokens'
+ *                     positions are written, every kv head.
+ * Asynchronous on `stream`, no allocation.  Two tokens at one position leave
+ * either's values.  Errors: TA_ERR_INVALID_ARG, TA_ERR_ALIGNMENT,
+ * TA_ERR_HOST_ONLY_PLAN (the destinations live in the device plan),
+ * TA_ERR_CUDA. */
+tree_attn_status tree_attn_append_kv(tree_attn_plan_t plan, const void* k_new,
+                                     const void* v_new, void* k_pages, void* v_pages,
+                                     void* stream);
+
 /* Size of the scratch array compiled into the library for
  * tree_attn_run_static(): 32 MiB, held on every GPU where that entry point's
  * code is loaded, until the process exits. */

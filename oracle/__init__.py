@@ -6,7 +6,8 @@ CPU-baseline / reference legs of ``bench.py`` may import it; the product path
 (``tree_structured_decode_gb300``) never does, and shares no code with it.
 
 Modules
-  attention  the tree-attention definition (fp64) and the log-sum-exp merge.
+  attention  the tree-attention definition (fp64), the log-sum-exp merge and
+             the append of the query tokens' own K/V before attention.
   planner    the greedy binary edge assignment and grouping plan, written
              from the FastTree review page (Algorithm 1 and its cost model),
              used to check the native planner decision by decision.
@@ -24,6 +25,7 @@ from .attention import (  # noqa: F401
     tree_attention_spec,
     merge_partials,
     attention_rows,
+    append_kv,
 )
 from .planner import (  # noqa: F401
     PlannerOptions,

@@ -171,3 +171,31 @@ def merge_partials(outs, lses):
     o = np.where(finite[..., None], o, 0.0)
     lse = np.where(finite, m_safe + np.log(den_safe), -np.inf)
     return o, lse
+
+
+def append_kv(node_kv_len, node_page_offsets, node_pages, query_node, query_kv_end,
+              k_pages, v_pages, k_new, v_new):
+    """The step before attention in a decode step: every query token's own K
+    and V go to its own position of the paged cache.
+
+    Decode appends each new token's K/V to its node before attending, so a
+    node's length already counts its query tokens, and a query token's own
+    token is the last it sees: position e - 1 of its node, e being its
+    visible end (DeFT notes page, "Tree attention definition"; the TGI
+    FlashDecoding pull request gives each query token its own KV slot).  A
+    token with e = 0 owns no position.  Returns new page pools (copies):
+    k_pages[page, :, slot, :] = k_new[t] with page and slot of that position,
+    likewise for V; everything else is unchanged.  Arrays are numpy (any
+    dtype); tokens are applied in order."""
+    k_out, v_out = np.array(k_pages, copy=True), np.array(v_pages, copy=True)
+    ps = k_out.shape[2]
+    for t, u in enumerate(query_node):
+        u = int(u)
+        e = int(node_kv_len[u]) if query_kv_end is None else int(query_kv_end[t])
+        if e < 1:
+            continue
+        pos = e - 1
+        page = int(node_pages[int(node_page_offsets[u]) + pos // ps])
+        k_out[page, :, pos % ps, :] = k_new[t]
+        v_out[page, :, pos % ps, :] = v_new[t]
+    return k_out, v_out

@@ -106,6 +106,16 @@ def test_run_on_host_only_plan_fails_without_touching_the_gpu():
     assert _abi.STATUS_NAMES[st] == "TA_ERR_HOST_ONLY_PLAN"
 
 
+def test_append_on_host_only_plan_fails_without_touching_the_gpu():
+    spec = W.random_tree(4, n_nodes=3)
+    p = _plan(spec)
+    f = [ctypes.c_void_p(16)] * 4
+    st = ta.load_library().tree_attn_append_kv(p._handle, *f, ctypes.c_void_p(0))
+    assert _abi.STATUS_NAMES[st] == "TA_ERR_HOST_ONLY_PLAN"
+    st = ta.load_library().tree_attn_append_kv(None, *f, ctypes.c_void_p(0))
+    assert _abi.STATUS_NAMES[st] == "TA_ERR_INVALID_ARG"
+
+
 def test_empty_query_set_and_zero_length_nodes_plan():
     spec = W._finish("empty", [-1, 0], [0, 0], [], [], 4, 2, 64, seed=0)
     with _plan(spec) as p:

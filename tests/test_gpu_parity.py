@@ -207,3 +207,16 @@ def test_tokens_with_more_partials_than_one_merge_round():
     assert stats["n_partials"] >= 32 * spec.n_queries
     ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
     compare(out, lse, ref, ref_lse)
+
+
+# ----------------------------------------------------------------- draft token trees
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (64, 4)])
+def test_draft_token_tree_verification(hq, hkv):
+    # six sequences below one prompt, each with a 3-level draft-token tree
+    # (branching 3: 39 draft tokens); every draft token is a one-token node
+    # that sees the prompt, its sequence and its draft ancestors
+    spec = W.token_tree(700, 6, 130, 3, 3, hq, hkv, 128, seed=hq)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, _ = run_gpu(spec, q, k, v)
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    compare(out, lse, ref, ref_lse)

@@ -120,3 +120,10 @@ def test_kv_head_packing_matches_reference(hq, hkv, ntok):
     spec = W._finish("heads", [-1] + [0] * 6, lens, qnode, qend, hq, hkv, 128, seed=11)
     for opt in ({}, {"split_tokens": 128}, {"no_pack": 1}, {"num_sms": 8}):
         _same(spec, **opt)
+
+
+@pytest.mark.parametrize("depth,branching,hq,hkv", [(3, 3, 32, 8), (2, 4, 64, 4), (4, 2, 8, 8)])
+def test_draft_token_trees_match_reference(depth, branching, hq, hkv):
+    spec = W.token_tree(500, 4, 90, depth, branching, hq, hkv, 128, seed=depth)
+    for opt in ({}, {"split_tokens": 128}, {"gamma": 2000}):
+        _same(spec, **opt)

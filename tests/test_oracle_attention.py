@@ -282,3 +282,35 @@ def test_page_order_is_irrelevant():
     spec.node_pages = perm[spec.node_pages].astype(np.int32)
     out2, lse2 = _run_spec(spec, q, k2, v2)
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_token_tree_verification_equals_masked_flat_attention():
+    # Tree verification with a draft-token tree: the oracle on the tree of
+    # one-token nodes equals dense attention over the flattened sequence
+    # [prompt, context, drafts] with the usual verification mask (a draft
+    # sees the prompt, its context and its draft ancestors), written here
+    # directly from that mask.
+    spec = W.token_tree(40, 2, 9, 3, 2, 4, 2, 16, seed=5)
+    q, k, v = W.make_tensors(spec, seed=5)
+    q, kp, vp = _np(q), _np(k), _np(v)
+    out, lse = oracle.tree_attention_spec(spec, q, kp, vp)
+    # flatten node by node (node ids are in DFS-compatible creation order)
+    order = list(range(spec.n_nodes))
+    tok_node, tok_k, tok_v = [], [], []
+    for u in order:
+        n = int(spec.node_kv_len[u])
+        tok_node += [u] * n
+        tok_k.append(oracle.gather_node_kv(kp, spec.node_page_offsets, spec.node_pages, u, n))
+        tok_v.append(oracle.gather_node_kv(vp, spec.node_page_offsets, spec.node_pages, u, n))
+    K, V = np.concatenate(tok_k), np.concatenate(tok_v)
+    anc = {u: set(oracle.node_path(spec.parent, u)) for u in order}
+    r = spec.n_q_heads // spec.n_kv_heads
+    s = 1.0 / np.sqrt(spec.head_dim)
+    for t in range(spec.n_queries):
+        u = int(spec.query_node[t])
+        mask = np.array([tn in anc[u] for tn in tok_node])
+        for h in range(spec.n_q_heads):
+            sc = s * (K[mask, h // r, :] @ q[t, h])
+            w = np.exp(sc - sc.max())
+            np.testing.assert_allclose(out[t, h], (w / w.sum()) @ V[mask, h // r, :], atol=1e-12)
+            np.testing.assert_allclose(lse[t, h], sc.max() + np.log(w.sum()), atol=1e-12)

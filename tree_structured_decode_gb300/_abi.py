@@ -19,7 +19,7 @@ EXPORTS = (
     "tree_attn_options_init", "tree_attn_plan", "tree_attn_run", "tree_attn_device_status",
     "tree_attn_plan_describe", "tree_attn_plan_get_stats", "tree_attn_plan_destroy",
     "tree_attn_status_string", "tree_attn_last_error", "tree_attn_profile_enable",
-    "tree_attn_profile_read", "tree_attn_run_static",
+    "tree_attn_profile_read", "tree_attn_run_static", "tree_attn_append_kv",
 )
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -95,6 +95,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.tree_attn_run.restype = ctypes.c_int
     lib.tree_attn_run_static.argtypes = [ctypes.c_void_p] * 7
     lib.tree_attn_run_static.restype = ctypes.c_int
+    lib.tree_attn_append_kv.argtypes = [ctypes.c_void_p] * 6
+    lib.tree_attn_append_kv.restype = ctypes.c_int
     lib.tree_attn_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _I32P]
     lib.tree_attn_device_status.restype = ctypes.c_int
     lib.tree_attn_profile_enable.argtypes = [ctypes.c_void_p, ctypes.c_int32]

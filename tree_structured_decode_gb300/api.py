@@ -126,6 +126,22 @@ class Plan:
         check(st, "tree_attn_run")
         return out, lse
 
+    def append_kv(self, k_new, v_new, k_pages, v_pages, stream=None):
+        """``tree_attn_append_kv``: write every query token's key and value
+        (bf16 ``[n_query_tokens, n_kv_heads, head_dim]``) into its own
+        position of the page pools (its visible end - 1), in place."""
+        import torch
+
+        for name, t in (("k_new", k_new), ("v_new", v_new), ("k_pages", k_pages),
+                        ("v_pages", v_pages)):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+        st = self._lib.tree_attn_append_kv(
+            self._handle, ctypes.c_void_p(k_new.data_ptr()), ctypes.c_void_p(v_new.data_ptr()),
+            ctypes.c_void_p(k_pages.data_ptr()), ctypes.c_void_p(v_pages.data_ptr()),
+            _stream_handle(stream))
+        check(st, "tree_attn_append_kv")
+
     def run_static(self, q, k_pages, v_pages, out, lse, stream=None) -> int:
         """tree_attn_run_static(): run without any device allocation (the
         library's fixed scratch holds the tables and partial results).  For

@@ -87,7 +87,42 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
   }
 }
 
+// One thread per 16 bytes of a (token, kv head) row of K or V: the row of
+// token t, head h goes to page dst[t] / 16, slot dst[t] % 16, head h.
+__global__ void __launch_bounds__(256) append_kv_kernel(const uint4* k_new, const uint4* v_new,
+                                                        const int32_t* dst, int nq, int hkv,
+                                                        int chunks, uint4* k_pages,
+                                                        uint4* v_pages) {
+  const long long per_tok = (long long)hkv * chunks;  // 16-byte chunks of one token's K (or V)
+  const long long n = 2 * (long long)nq * per_tok;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const bool is_v = i >= (long long)nq * per_tok;
+    const long long j = is_v ? i - (long long)nq * per_tok : i;
+    const int t = (int)(j / per_tok);
+    const int h = (int)((j / chunks) % hkv), c = (int)(j % chunks);
+    const int where = __ldg(dst + t);
+    if (where < 0) continue;
+    const long long row = ((long long)(where >> 4) * hkv + h) * 16 + (where & 15);
+    (is_v ? v_pages : k_pages)[row * chunks + c] = __ldg((is_v ? v_new : k_new) + j);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_append_kv(const uint16_t* k_new, const uint16_t* v_new, const int32_t* dst,
+                             int nq, int hkv, int d, uint16_t* k_pages, uint16_t* v_pages,
+                             cudaStream_t s) {
+  if (nq == 0) return cudaSuccess;
+  const int chunks = d * 2 / 16;
+  const long long n = 2LL * nq * hkv * chunks;
+  const int blocks = (int)((n + 255) / 256 < 152 * 8 ? (n + 255) / 256 : 152 * 8);
+  append_kv_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(k_new),
+                                          reinterpret_cast<const uint4*>(v_new), dst, nq, hkv,
+                                          chunks, reinterpret_cast<uint4*>(k_pages),
+                                          reinterpret_cast<uint4*>(v_pages));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;

@@ -68,5 +68,10 @@ cudaError_t launch_tree_attention(const AttnParams& p, int d, int grid, int num_
                                   cudaStream_t s);
 // Launch the log-sum-exp merge of partial results.
 cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s);
+// Copy each query token's new K and V (bf16 [nq][hkv][d]) into its page slot
+// (dst[t] = page * 16 + slot, or -1 to skip) of the paged cache.
+cudaError_t launch_append_kv(const uint16_t* k_new, const uint16_t* v_new, const int32_t* dst,
+                             int nq, int hkv, int d, uint16_t* k_pages, uint16_t* v_pages,
+                             cudaStream_t s);
 
 }  // namespace ta

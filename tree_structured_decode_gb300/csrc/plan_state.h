@@ -28,6 +28,7 @@ struct tree_attn_plan_s {
   int32_t* d_merge_cnt = nullptr;
   size_t merge_cnt_bytes = 0;
   const int32_t* d_tok_poff = nullptr;
+  const int32_t* d_append = nullptr;  // per query token: page * 16 + slot of its own KV, or -1
   double plan_ms = 0.0;
   bool profiling = false;
   bool profiled_run = false;

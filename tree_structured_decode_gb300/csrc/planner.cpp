@@ -153,6 +153,16 @@ tree_attn_status build_host_plan(
 
   HostPlan& p = *P;
   p = HostPlan();
+  // Each query token's own KV position: the last position it sees in its
+  // node (decode appends the token's K/V before attention).
+  p.append_dst.assign(nq, -1);
+  for (int t = 0; t < nq; ++t) {
+    const int u = query_node[t];
+    const int e = query_kv_end ? query_kv_end[t] : node_kv_len[u];
+    if (e >= 1)
+      p.append_dst[t] = node_pages[node_page_offsets[u] + (e - 1) / kPageSize] * kPageSize +
+                        (e - 1) % kPageSize;
+  }
   p.n_nodes = n;
   p.nq = nq;
   p.hq = hq;

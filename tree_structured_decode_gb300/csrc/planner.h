@@ -95,6 +95,8 @@ struct HostPlan {
   std::vector<int32_t> chunk_lo, chunk_hi;
   int64_t chunk_blocks = 0;
   std::vector<int32_t> pcount, poff;          // per query token
+  std::vector<int32_t> append_dst;            // per query token: page * 16 + slot of its own
+                                              // position (visible end - 1), or -1
   int64_t n_partials = 0;
   std::vector<int32_t> merge_tok;             // tokens with >= 2 partials
   std::vector<UnitDesc> units;                // in schedule order (CTA-major)

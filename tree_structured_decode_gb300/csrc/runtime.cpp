@@ -73,7 +73,7 @@ tree_attn_status upload(tree_attn_plan_s* P) {
     size_t bytes;
     size_t off;
   };
-  Sec secs[7] = {
+  Sec secs[8] = {
       {h.units.data(), h.units.size() * sizeof(ta::UnitDesc), 0},
       {blocks.data(), blocks.size() * sizeof(int2), 0},
       {gt.data(), gt.size() * sizeof(ta::GroupTok), 0},
@@ -81,6 +81,7 @@ tree_attn_status upload(tree_attn_plan_s* P) {
       {merge.data(), merge.size() * sizeof(ta::MergeItem), 0},
       {nullptr, 16 * sizeof(int32_t), 0},  // error word(s)
       {h.poff.data(), h.poff.size() * sizeof(int32_t), 0},
+      {h.append_dst.data(), h.append_dst.size() * sizeof(int32_t), 0},
   };
   size_t off = 0;
   for (auto& s : secs) {
@@ -106,6 +107,7 @@ tree_attn_status upload(tree_attn_plan_s* P) {
   P->d_merge = reinterpret_cast<const ta::MergeItem*>(b + secs[4].off);
   P->d_err = reinterpret_cast<int32_t*>(b + secs[5].off);
   P->d_tok_poff = reinterpret_cast<const int32_t*>(b + secs[6].off);
+  P->d_append = reinterpret_cast<const int32_t*>(b + secs[7].off);
 
   const size_t np = (size_t)h.n_partials * h.hq;
   const size_t o_bytes = align_up(np * h.d * sizeof(uint16_t), 256);  // fp16 partial O
@@ -225,6 +227,27 @@ tree_attn_status tree_attn_plan(const int32_t* parent, int32_t n_nodes, const in
   }
   P->plan_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
   *plan_out = P;
+  return TA_OK;
+}
+
+tree_attn_status tree_attn_append_kv(tree_attn_plan_t P, const void* k_new, const void* v_new,
+                                     void* k_pages, void* v_pages, void* stream) {
+  g_last_error.clear();
+  if (!P) return set_err(TA_ERR_INVALID_ARG, "plan is NULL");
+  if (P->host_only) return set_err(TA_ERR_HOST_ONLY_PLAN, "plan was made with host_only = 1");
+  const ta::HostPlan& h = P->hp;
+  if (h.nq == 0) return TA_OK;
+  if (!k_new || !v_new || !k_pages || !v_pages)
+    return set_err(TA_ERR_INVALID_ARG, "k_new, v_new, k_pages and v_pages must be non-NULL");
+  auto mis = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
+  if (mis(k_new) || mis(v_new) || mis(k_pages) || mis(v_pages))
+    return set_err(TA_ERR_ALIGNMENT, "k_new, v_new, k_pages and v_pages must be 16-byte aligned");
+  cudaError_t e = ta::launch_append_kv(static_cast<const uint16_t*>(k_new),
+                                       static_cast<const uint16_t*>(v_new), P->d_append, h.nq,
+                                       h.hkv, h.d, static_cast<uint16_t*>(k_pages),
+                                       static_cast<uint16_t*>(v_pages),
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_err(e, "append launch");
   return TA_OK;
 }
 

@@ -171,6 +171,34 @@ def two_level(root_len, n_leaves, leaf_len, hq, hkv, d, seed=0, name="two_level"
     return _finish(name, parent, lens, qn, qe, hq, hkv, d, seed)
 
 
+def token_tree(prompt_len, n_ctx, ctx_len, depth, branching, hq, hkv, d, seed=0,
+               name="token_tree"):
+    """Speculative token trees for tree verification: a shared prompt, n_ctx
+    sequences of ctx_len generated tokens below it, and under each a tree of
+    draft tokens (depth levels, `branching` children per token).  Every draft
+    token is its own one-token node and one query token that sees its node
+    in full, so it attends to the prompt, its sequence and its draft-tree
+    ancestors: an arbitrary intra-leaf token tree expressed as tree
+    topology."""
+    parent, lens = [-1], [prompt_len]
+    qn, qe = [], []
+    for _ in range(n_ctx):
+        parent.append(0)
+        lens.append(ctx_len)
+        level = [len(parent) - 1]
+        for _ in range(depth):
+            nxt = []
+            for par in level:
+                for _ in range(branching):
+                    parent.append(par)
+                    lens.append(1)
+                    qn.append(len(parent) - 1)
+                    qe.append(1)
+                    nxt.append(len(parent) - 1)
+            level = nxt
+    return _finish(name, parent, lens, qn, qe, hq, hkv, d, seed)
+
+
 def config_tiny(seed=1):
     """Root 256 KV tokens, 4 leaves of 32; 4 q heads = 4 kv heads, d = 64."""
     return two_level(256, 4, 32, 4, 4, 64, seed, name="tiny")
