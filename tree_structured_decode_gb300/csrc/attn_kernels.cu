@@ -19,9 +19,9 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // One warp per (merge token, q head).  The partials are read G at a time
 // (lse and the lane's columns of every O row in flight together) and folded
 // online: the running max M only grows, and the sums kept so far are scaled
-// by 2^(M_old - M_new) when it does.  G = 8 keeps the registers low for
-// many short merges; plans whose tokens have more partials use G = 24 so a
-// token takes one round of loads.
+// by 2^(M_old - M_new) when it does.  The launch picks G from the plan's
+// largest partial count (4, 8 or 24) so that a token takes one round of
+// loads where possible, with as few registers as that allows.
 template <int D, int G, int kMinBlocks>
 __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeParams p) {
   constexpr int EPL = D / 32;  // 4 or 2 columns per lane
@@ -128,17 +128,22 @@ cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
   const long long warps = (long long)p.n_items * p.hq;
   const int blocks = (int)((warps + 7) / 8 < 152 * 16 ? (warps + 7) / 8 : 152 * 16);
-  const bool wide_rounds = p.max_count > 8;  // tokens with up to 24 partials: one round
+  // one round of loads per token where possible; fewer partials per round
+  // leave registers for more resident warps
   if (d == 128) {
-    if (wide_rounds)
+    if (p.max_count > 8)
       lse_merge_kernel<128, 24, 1><<<blocks, 256, 0, s>>>(p);
-    else
+    else if (p.max_count > 4)
       lse_merge_kernel<128, 8, 4><<<blocks, 256, 0, s>>>(p);
-  } else {
-    if (wide_rounds)
-      lse_merge_kernel<64, 24, 1><<<blocks, 256, 0, s>>>(p);
     else
+      lse_merge_kernel<128, 4, 6><<<blocks, 256, 0, s>>>(p);
+  } else {
+    if (p.max_count > 8)
+      lse_merge_kernel<64, 24, 1><<<blocks, 256, 0, s>>>(p);
+    else if (p.max_count > 4)
       lse_merge_kernel<64, 8, 4><<<blocks, 256, 0, s>>>(p);
+    else
+      lse_merge_kernel<64, 4, 6><<<blocks, 256, 0, s>>>(p);
   }
   return cudaGetLastError();
 }
