@@ -142,6 +142,16 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sh
   }
 }
 
+// wait_bar for a whole (converged) warp: true only if every lane's wait
+// succeeded, so the warp stays converged.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Shared& sh,
+                                          int32_t* err, long long limit_ns) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, sh, err, limit_ns));
+}
+__device__ __forceinline__ bool warp_aborted(const Shared& sh) {
+  return __any_sync(0xffffffffu, *sh.abort_flag != 0);
+}
+
 // Wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long long limit_ns) {
   const uint64_t t0 = ptx::globaltimer();
@@ -157,14 +167,15 @@ __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x 
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
 // ============================================================== producers
-// One thread streams K (kIsV false) or V (true) of every tile of the CTA's
-// units into the stage ring.
+// One warp streams K (kIsV false) or V (true) of every tile of the CTA's
+// units into the stage ring.  The whole warp runs the loop (its values stay
+// warp-uniform); one elected lane issues each copy.
 template <int D, bool kIsV>
 __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int u1,
                          const Shared& sh, const Bars<D>& B) {
   using C = Cfg<D>;
   uint32_t g = 0;
-  if (!kIsV && p.debug_stuck_wait) wait_bar(B.never(), 0, sh, p.err, p.wait_timeout_ns);
+  if (!kIsV && p.debug_stuck_wait) warp_wait(B.never(), 0, sh, p.err, p.wait_timeout_ns);
   uint32_t filled[C::kStages];  // 1 + tile index of the last fill issued per stage
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) filled[s] = 0;
@@ -180,16 +191,17 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
       for (int bb = 0; bb < kBpt; ++bb) page[bb] = bb < nb ? __ldg(&p.blocks[b0 + bb].x) : 0;
       const uint32_t full = kIsV ? B.vfull(s) : B.kfull(s);
       if (g >= (uint32_t)C::kStages &&
-          !wait_bar(kIsV ? B.vempty(s) : B.kempty(s), ((g / C::kStages) + 1) & 1, sh, p.err,
-                    p.wait_timeout_ns))
+          !warp_wait(kIsV ? B.vempty(s) : B.kempty(s), ((g / C::kStages) + 1) & 1, sh, p.err,
+                     p.wait_timeout_ns))
         continue;
-      if (*sh.abort_flag) continue;
-      ptx::mbar_arrive_expect_tx(full, (uint32_t)nb * C::kBlockBytes);
+      if (warp_aborted(sh)) continue;
+      const bool leader = ptx::elect_one();
+      if (leader) ptx::mbar_arrive_expect_tx(full, (uint32_t)nb * C::kBlockBytes);
       const int kvh = u.kvh, hstep = (u.path & kUnitHeads) ? 1 : 0;  // page bb's kv head
       const uint32_t dst = sh.base + (kIsV ? C::kOffV : C::kOffK) + s * C::kTileBytes;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
-        if (bb < nb) {
+        if (bb < nb && leader) {
           if constexpr (!kIsV) {
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h)
@@ -207,7 +219,7 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
         if (t == s) filled[t] = g + 1;
     }
   }
-  if (*sh.abort_flag) {
+  if (warp_aborted(sh)) {
     // let the last copy issued into every stage land before the CTA exits
 #pragma unroll
     for (int s = 0; s < C::kStages; ++s)
@@ -233,20 +245,20 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       g += T;
       continue;
     }
-    const bool qok = wait_bar(B.q_full(0), nu & 1, sh, p.err, p.wait_timeout_ns);
+    const bool qok = warp_wait(B.q_full(0), nu & 1, sh, p.err, p.wait_timeout_ns);
     ptx::tc_fence_after();
     const uint32_t o_tmem = tmem + 128;
     auto issue_pv = [&](int jj) {
       const int pb = (gm + jj) & 1;  // P(jj) sits in the first 32 columns of S buffer pb
-      bool ok = wait_bar(B.p_full(pb), ((gm + jj) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
+      bool ok = warp_wait(B.p_full(pb), ((gm + jj) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
       // the first P.V of a unit overwrites O: the previous unit's epilogue
       // must have read it
-      if (jj == 0 && nu > 0) ok = wait_bar(B.o_empty(), (nu - 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
+      if (jj == 0 && nu > 0) ok = warp_wait(B.o_empty(), (nu - 1) & 1, sh, p.err, p.wait_timeout_ns) && ok;
       const int s = (g + jj) % C::kStages;
-      ok = ok && wait_bar(B.vfull(s), ((g + jj) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+      ok = ok && warp_wait(B.vfull(s), ((g + jj) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
       ptx::tc_fence_after();
       const int nbk = min(kBpt, u.blk1 - (u.blk0 + kBpt * jj));
-      if (ok && !*sh.abort_flag) {
+      if (ok && !warp_aborted(sh) && ptx::elect_one()) {
         // descriptors: the 14-bit start address field (16-byte units) of the
         // stage's base descriptor plus the page offset (no carry: the shared
         // window is below 256 KB)
@@ -256,17 +268,19 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
                            C::kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
         issued = true;
       }
-      ptx::mma_commit(B.vempty(s));
-      ptx::mma_commit(B.pv_done(pb));
+      if (ptx::elect_one()) {
+        ptx::mma_commit(B.vempty(s));
+        ptx::mma_commit(B.pv_done(pb));
+      }
     };
     for (int j = 0; j < T; ++j) {
       const int s = (g + j) % C::kStages;
       const int sb = (gm + j) & 1;
-      bool ok = qok && wait_bar(B.kfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+      bool ok = qok && warp_wait(B.kfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
       // S buffer sb holds P of the tile two back until that P.V has completed
-      ok = ok && wait_bar(B.pv_done(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
+      ok = ok && warp_wait(B.pv_done(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
       ptx::tc_fence_after();
-      if (ok && !*sh.abort_flag) {
+      if (ok && !warp_aborted(sh) && ptx::elect_one()) {
         const uint64_t dk = ptx::sdesc_sw128(sh.base + C::kOffK + s * C::kTileBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -277,18 +291,20 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
         }
         issued = true;
       }
-      ptx::mma_commit(B.s_full(sb));
-      ptx::mma_commit(B.kempty(s));
+      if (ptx::elect_one()) {
+        ptx::mma_commit(B.s_full(sb));
+        ptx::mma_commit(B.kempty(s));
+      }
       if (j > 0) issue_pv(j - 1);
     }
     issue_pv(T - 1);
-    ptx::mma_commit(B.o_full());
+    if (ptx::elect_one()) ptx::mma_commit(B.o_full());
     g += T;
     gm += T;
     ++nu;
   }
-  if (*sh.abort_flag && issued) {
-    ptx::mma_commit(B.drain());
+  if (warp_aborted(sh) && __any_sync(0xffffffffu, issued)) {
+    if (ptx::elect_one()) ptx::mma_commit(B.drain());
     drain_wait(B.drain(), 0, kDrainLimitNs);
   }
 }
@@ -1051,11 +1067,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else {
     ptx::setmaxnreg_dec<kIssueRegs>();
     if (warp == kProducerWarp) {
-      if (lane == 0) producer<D, false>(&tmk, p, u0, u1, sh, B);
+      producer<D, false>(&tmk, p, u0, u1, sh, B);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_issuer<D>(p, u0, u1, sh, B, tmem);
+      mma_issuer<D>(p, u0, u1, sh, B, tmem);
     } else if (warp == kVProducerWarp) {
-      if (lane == 0) producer<D, true>(&tmv, p, u0, u1, sh, B);
+      producer<D, true>(&tmv, p, u0, u1, sh, B);
     }  // warp 7 only completes the warpgroup
     __syncwarp();
   }
