@@ -328,7 +328,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 
 // One thread folds row (tok, h).  Returns nothing; no-op unless last.
 template <int D>
-__device__ void merge_row_thread(const AttnParams& p, const GroupTok& gt, int h) {
+__device__ __noinline__ void merge_row_thread(const AttnParams& p, const GroupTok& gt, int h) {
   const int idx = gt.tok * p.hq + h;
   __threadfence();
   if (atomicAdd(p.merge_cnt + idx, 1) != gt.pcount() - 1) return;
@@ -380,7 +380,7 @@ __device__ void merge_row_thread(const AttnParams& p, const GroupTok& gt, int h)
 
 // A warp folds row (tok, h), lanes over d (lane holds EPL columns).
 template <int D>
-__device__ void merge_row_warp(const AttnParams& p, const GroupTok& gt, int h, int lane) {
+__device__ __noinline__ void merge_row_warp(const AttnParams& p, const GroupTok& gt, int h, int lane) {
   constexpr int EPL = D / 32;
   const int idx = gt.tok * p.hq + h;
   int last = 0;
@@ -475,10 +475,13 @@ __device__ __forceinline__ float transpose_sum16(float (&v)[16], int lane) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-// CUDA-core consumer for a thin unit (<= 8 rows).
+// CUDA-core consumer for a thin unit (<= 8 rows).  Like the fused-merge
+// folds, kept out of line (about half of the kernel's code), so that the
+// tensor-core tile loop of the compute warps stays compact in the
+// instruction caches.
 template <int D>
-__device__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, int T,
-                          const Shared& sh, const Bars<D>& B) {
+__device__ __noinline__ void simt_unit(const AttnParams& p, const UnitDesc& u, uint32_t g, int T,
+                                       const Shared& sh, const Bars<D>& B) {
   using C = Cfg<D>;
   constexpr int EPL = D / 32;
   constexpr int RB = kSimtTileRows;
