@@ -982,13 +982,17 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     if (ok && wact) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse2 = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
+      // O in 64-column halves: one TMEM round trip per half
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float t32[32];
-        ptx::tmem_ld32(o_tmem + c * 32, t32);
+      for (int c = 0; c < D / 32; c += 2) {
+        float o0[32], o1[32];
+        ptx::tmem_ld32(o_tmem + c * 32, o0);
+        ptx::tmem_ld32(o_tmem + c * 32 + 32, o1);
         ptx::tmem_wait_ld();
-        if (row_ok && !*sh.abort_flag)
-          write_row_cols<D, 32>(p, u, u.row0 + tid, gt_row, t32, c * 32, inv, lse2, c == 0);
+        if (row_ok && !*sh.abort_flag) {
+          write_row_cols<D, 32>(p, u, u.row0 + tid, gt_row, o0, c * 32, inv, lse2, c == 0);
+          write_row_cols<D, 32>(p, u, u.row0 + tid, gt_row, o1, c * 32 + 32, inv, lse2, false);
+        }
       }
     }
     ptx::tc_fence_before();
