@@ -16,45 +16,50 @@ namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// One warp per (merge token, q head).  The partials are read G at a time
-// (lse and the lane's columns of every O row in flight together) and folded
-// online: the running max M only grows, and the sums kept so far are scaled
-// by 2^(M_old - M_new) when it does.  The launch picks G from the plan's
+// Two (merge token, q head) rows per warp, 16 lanes each: a lane holds D / 16
+// columns (one 16-byte fp16 load per partial row for D = 128).  The partials
+// are read G at a time (lse and the lane's columns of G partial rows in
+// flight together, kept as packed fp16 until folded) and folded online: the
+// running max M only grows, and the sums kept so far are scaled by
+// 2^(M_old - M_new) when it does.  The launch picks G from the plan's
 // largest partial count (4, 8 or 24) so that a token takes one round of
 // loads where possible, with as few registers as that allows.
 template <int D, int G, int kMinBlocks>
 __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeParams p) {
-  constexpr int EPL = D / 32;  // 4 or 2 columns per lane
-  const int lane = threadIdx.x & 31;
+  constexpr int EPL = D / 16;  // 8 or 4 columns per lane
+  constexpr int NW = EPL / 2;  // fp16 pairs per lane
+  const int lane = threadIdx.x & 31, sub = lane >> 4, l16 = lane & 15;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int total = p.n_items * p.hq;
-  for (int idx = gw; idx < total; idx += nw) {
+  for (int r0 = 2 * gw; r0 < total; r0 += 2 * nw) {
+    const int idx = r0 + sub;
+    if (idx >= total) continue;
     const MergeItem it = p.items[idx / p.hq];
     const int h = idx % p.hq;
     const float* lse_h = p.part_lse + (size_t)it.poff * p.hq + h;  // partial k at lse_h[k * hq]
-    const uint16_t* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + lane * EPL;  // fp16
+    const uint16_t* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + l16 * EPL;  // fp16
     float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
     for (int k0 = 0; k0 < it.count; k0 += G) {
-      float w[G], v[G][EPL];
+      float w[G];
+      uint32_t v[G][NW];
 #pragma unroll
       for (int q = 0; q < G; ++q) {
         const int k = k0 + q;
         w[q] = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) v[q][e] = 0.f;
+        for (int e = 0; e < NW; ++e) v[q][e] = 0u;
         if (k < it.count) {
           w[q] = __ldcg(lse_h + (size_t)k * p.hq);
           const uint16_t* src = o_h + (size_t)k * p.hq * D;
-          if constexpr (EPL == 4) {
-            const uint2 t = __ldcg(reinterpret_cast<const uint2*>(src));
-            const float2 a = ptx::unpack_f16(t.x), b = ptx::unpack_f16(t.y);
-            v[q][0] = a.x, v[q][1] = a.y, v[q][2] = b.x, v[q][3] = b.y;
+          if constexpr (NW == 4) {
+            const uint4 t = __ldcg(reinterpret_cast<const uint4*>(src));
+            v[q][0] = t.x, v[q][1] = t.y, v[q][2] = t.z, v[q][3] = t.w;
           } else {
-            const float2 a = ptx::unpack_f16(__ldcg(reinterpret_cast<const unsigned int*>(src)));
-            v[q][0] = a.x, v[q][1] = a.y;
+            const uint2 t = __ldcg(reinterpret_cast<const uint2*>(src));
+            v[q][0] = t.x, v[q][1] = t.y;
           }
         }
       }
@@ -72,17 +77,20 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
         const float wq = exp2f(w[q] - m_new);  // 0 for absent or empty partials
         den += wq;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wq, v[q][e], acc[e]);
+        for (int e = 0; e < NW; ++e) {
+          const float2 f = ptx::unpack_f16(v[q][e]);
+          acc[2 * e] = fmaf(wq, f.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(wq, f.y, acc[2 * e + 1]);
+        }
       }
       M = m_new;
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    float* dst = p.out + ((size_t)it.tok * p.hq + h) * D + lane * EPL;
-    if constexpr (EPL == 4)
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-    else
-      *reinterpret_cast<float2*>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
-    if (lane == 0 && p.lse)
+    float* dst = p.out + ((size_t)it.tok * p.hq + h) * D + l16 * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 4)
+      *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv);
+    if (l16 == 0 && p.lse)
       p.lse[(size_t)it.tok * p.hq + h] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
   }
 }
@@ -126,7 +134,7 @@ cudaError_t launch_append_kv(const uint16_t* k_new, const uint16_t* v_new, const
 
 cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
-  const long long warps = (long long)p.n_items * p.hq;
+  const long long warps = ((long long)p.n_items * p.hq + 1) / 2;  // two rows per warp
   const int blocks = (int)((warps + 7) / 8 < 152 * 16 ? (warps + 7) / 8 : 152 * 16);
   // one round of loads per token where possible; fewer partials per round
   // leave registers for more resident warps
@@ -134,14 +142,14 @@ cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
     if (p.max_count > 8)
       lse_merge_kernel<128, 24, 1><<<blocks, 256, 0, s>>>(p);
     else if (p.max_count > 4)
-      lse_merge_kernel<128, 8, 4><<<blocks, 256, 0, s>>>(p);
+      lse_merge_kernel<128, 8, 3><<<blocks, 256, 0, s>>>(p);
     else
-      lse_merge_kernel<128, 4, 6><<<blocks, 256, 0, s>>>(p);
+      lse_merge_kernel<128, 4, 4><<<blocks, 256, 0, s>>>(p);
   } else {
     if (p.max_count > 8)
       lse_merge_kernel<64, 24, 1><<<blocks, 256, 0, s>>>(p);
     else if (p.max_count > 4)
-      lse_merge_kernel<64, 8, 4><<<blocks, 256, 0, s>>>(p);
+      lse_merge_kernel<64, 8, 3><<<blocks, 256, 0, s>>>(p);
     else
       lse_merge_kernel<64, 4, 6><<<blocks, 256, 0, s>>>(p);
   }
