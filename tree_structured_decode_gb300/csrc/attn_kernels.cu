@@ -144,7 +144,7 @@ cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
     else if (p.max_count > 4)
       lse_merge_kernel<128, 8, 3><<<blocks, 256, 0, s>>>(p);
     else
-      lse_merge_kernel<128, 4, 4><<<blocks, 256, 0, s>>>(p);
+      lse_merge_kernel<128, 4, 5><<<blocks, 256, 0, s>>>(p);
   } else {
     if (p.max_count > 8)
       lse_merge_kernel<64, 24, 1><<<blocks, 256, 0, s>>>(p);
