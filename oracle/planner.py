@@ -240,30 +240,40 @@ def build_plan(parent, node_kv_len, node_page_offsets, node_pages, page_size,
         tile = o.mma_tile_rows if g["path"] == "mma" else o.simt_tile_rows
         g["qtiles"] = _ceil(g["rows"], tile)
     # Long-context split: chunk length in blocks, a multiple of one KV tile.
+    work = sum(len(g["blocks"]) * n_kv_heads * g["qtiles"] for g in groups)
     if o.split_tokens < 0:
         chunk = max([len(g["blocks"]) for g in groups] + [1])
         chunk = _ceil(chunk, bpt) * bpt
     elif o.split_tokens > 0:
         chunk = _ceil(_ceil(o.split_tokens, page_size), bpt) * bpt
     else:
-        work = sum(len(g["blocks"]) * n_kv_heads * g["qtiles"] for g in groups)
         target = _ceil(work, o.split_waves * o.num_sms)
         chunk = max(_ceil(o.min_split_tokens, page_size), _ceil(target, bpt) * bpt)
     chunk = max(chunk, bpt)
     # Thin tensor-core groups longer than a packable group (more than 8
-    # pages) run packed by kv head: a unit covers four kv heads, so the
-    # automatic split gives them a quarter of the chunk (not below the
-    # minimum split).
+    # pages) run packed by kv head: a unit covers four kv heads and one page
+    # of each per tile, so their chunks need no tile alignment.  The
+    # automatic split sizes them for one unit per CTA (two CTAs per SM): the
+    # plan's page-heads over the CTAs, a quarter of that in pages, not below
+    # half the minimum split, in near-equal chunks.
     def head_thin(g):
         return (not o.no_pack and g["path"] == "mma" and g["qtiles"] == 1
                 and g["rows"] <= 32 and 32 % r == 0 and n_kv_heads % 4 == 0
                 and len(g["blocks"]) > 8)
+    thin_chunk = max(_ceil(_ceil(o.min_split_tokens, page_size), 2),
+                     _ceil(work, 4 * o.num_sms * 2))
     for g in groups:
         nb = len(g["blocks"])
         cg = chunk
         if o.split_tokens == 0 and head_thin(g):
-            cg = max(_ceil(o.min_split_tokens, page_size), _ceil(chunk, 4))
-        if nb <= cg:
+            k = _ceil(nb, thin_chunk)
+            g["chunks"] = []
+            s = 0
+            for i in range(k):
+                n_i = nb // k + (1 if i < nb % k else 0)
+                g["chunks"].append([s, s + n_i])
+                s += n_i
+        elif nb <= cg:
             g["chunks"] = [[0, nb]]
         else:
             k = _ceil(nb, cg)

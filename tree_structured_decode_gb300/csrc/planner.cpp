@@ -296,6 +296,8 @@ tree_attn_status build_host_plan(
 
   // ------------------------------------------ long-span split (chunks)
   int64_t chunk;
+  int64_t work = 0;  // page-heads streamed, summed over query tiles
+  for (auto& g : p.groups) work += (int64_t)g.nblk * hkv * g.qtiles;
   if (opt.split_tokens < 0) {
     int64_t mx = 1;
     for (auto& g : p.groups) mx = std::max<int64_t>(mx, g.nblk);
@@ -303,8 +305,6 @@ tree_attn_status build_host_plan(
   } else if (opt.split_tokens > 0) {
     chunk = ceil_div(ceil_div(opt.split_tokens, page_size), kBlocksPerTile) * kBlocksPerTile;
   } else {
-    int64_t work = 0;
-    for (auto& g : p.groups) work += (int64_t)g.nblk * hkv * g.qtiles;
     int64_t target = ceil_div(work, (int64_t)std::max(1, opt.split_waves) * std::max(1, opt.num_sms));
     chunk = std::max(ceil_div(opt.min_split_tokens, page_size),
                      ceil_div(target, kBlocksPerTile) * kBlocksPerTile);
@@ -312,19 +312,33 @@ tree_attn_status build_host_plan(
   chunk = std::max<int64_t>(chunk, kBlocksPerTile);
   p.chunk_blocks = chunk;
   // Thin tensor-core groups longer than a packable group run packed by kv
-  // head (see the units below): a unit covers four kv heads, so the
-  // automatic split gives them a quarter of the chunk, not below the minimum.
+  // head (see the units below): a unit covers four kv heads and one page of
+  // each per tile, so its chunks need no tile alignment.  The automatic
+  // split sizes them for one unit per CTA (the page-heads of the whole plan
+  // over the CTAs, a quarter of that in pages), in near-equal chunks of at
+  // least half the minimum split: one long unit per CTA beats two short
+  // ones (each pays start-up and epilogue), and equal units leave no CTA
+  // with the tail.
   auto head_thin = [&](const GroupInfo& g) {
     return !opt.no_pack && g.path == kPathMma && g.qtiles == 1 && g.rows <= kPackMmaRows &&
            kPackMmaRows % r == 0 && hkv % kPackSlots == 0 && g.nblk > kPackMaxBlocks;
   };
+  const int64_t thin_chunk =
+      std::max(ceil_div(ceil_div(opt.min_split_tokens, page_size), 2),
+               ceil_div(work, (int64_t)kPackSlots * std::max(1, opt.num_sms) * kCtasPerSm));
   for (auto& g : p.groups) {
     g.chunk_off = (int32_t)p.chunk_lo.size();
     int64_t nb = g.nblk;
     int64_t cg = chunk;
-    if (opt.split_tokens == 0 && head_thin(g))
-      cg = std::max(ceil_div(opt.min_split_tokens, page_size), ceil_div(chunk, (int64_t)kPackSlots));
-    if (nb <= cg) {
+    if (opt.split_tokens == 0 && head_thin(g)) {
+      const int64_t k = ceil_div(nb, thin_chunk);
+      for (int64_t i = 0, s = 0; i < k; ++i) {
+        const int64_t len = nb / k + (i < nb % k ? 1 : 0);
+        p.chunk_lo.push_back((int32_t)s);
+        p.chunk_hi.push_back((int32_t)(s + len));
+        s += len;
+      }
+    } else if (nb <= cg) {
       p.chunk_lo.push_back(0);
       p.chunk_hi.push_back((int32_t)nb);
     } else {
