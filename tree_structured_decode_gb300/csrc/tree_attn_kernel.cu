@@ -12,8 +12,8 @@
 //    TMEM (double-buffered), the four compute warps read one row per thread,
 //    apply the mask and an online softmax (the running max is raised only
 //    when it grows by more than 2^8, so O is rarely rescaled), write P as
-//    bf16 to shared memory, and tcgen05 adds P V into the O accumulator in
-//    TMEM.
+//    bf16 over S in TMEM, and tcgen05 adds P V (P read from TMEM) into the O
+//    accumulator in TMEM.
 //  * CUDA cores (groups below the tensor-core row threshold, when it is
 //    raised): the compute warps split the tile's pages,
 //    lanes split the head dimension, and each warp keeps its own online
@@ -25,8 +25,8 @@
 //
 // Roles: warps 0-3 compute (thread i owns TMEM lane / query row i), warp 4
 // streams K and warp 6 streams V by TMA, warp 5 owns TMEM and issues
-// tcgen05.mma.  Every wait is
-// bounded: if one runs out the CTA records TA_DEVERR_TIMEOUT, stops issuing
+// tcgen05.mma; the issuing warps run converged, one elected lane issuing.
+// Every wait is bounded: if one runs out the CTA records TA_DEVERR_TIMEOUT, stops issuing
 // work, waits (bounded) for its copies and MMAs in flight, frees TMEM and
 // returns.
 #include <cuda.h>
@@ -69,19 +69,19 @@ struct Cfg {
   static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kQBytes = 128 * D * 2;          // the query tile
   static constexpr int kTileBytes = kTileTok * D * 2;  // K (or V) of one tile
-  static constexpr int kPBytes = 128 * kTileTok * 2;
+  static constexpr int kScratchBytes = 128 * kTileTok * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kOffScratch = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffScratch + kScratchBytes;
   static constexpr int kNumBars = 4 * kStages + 12;
   static constexpr int kOffML = kOffBar + kNumBars * 8 + 16;  // float [4][8][2]
   // the dynamic shared window starts 1024-byte aligned (checked at start)
   static constexpr int kSmem = kOffML + 4 * kSimtTileRows * 2 * 4;
   static_assert(kSmem <= 115 * 1024, "two CTAs per SM must fit in shared memory");
-  // the CUDA-core path combines its four warps' O in the (idle) P buffer
-  static_assert(4 * kSimtTileRows * D * 4 <= kPBytes, "combine scratch exceeds the P buffer");
+  // scratch of the CUDA-core path, where its four warps' O are combined
+  static_assert(4 * kSimtTileRows * D * 4 <= kScratchBytes, "combine scratch too small");
   // A stage holds K as [64-column half][tile token][128 B] (one box per page
   // and half; QK^T is one N = kTileTok MMA per 16 columns of d) and V as
   // [page][64-column half][16 tokens][128 B] (one box per page-head; P.V is
@@ -590,8 +590,8 @@ __device__ __noinline__ void simt_unit(const AttnParams& p, const UnitDesc& u, u
       ptx::mbar_arrive(B.vempty(s));
     }
   }
-  // combine the four warps' states (scratch in the P buffer, idle here)
-  float* sm_o = reinterpret_cast<float*>(sh.ptr + C::kOffP);   // [4][RB][D]
+  // combine the four warps' states in the scratch area
+  float* sm_o = reinterpret_cast<float*>(sh.ptr + C::kOffScratch);  // [4][RB][D]
   float* sm_ml = reinterpret_cast<float*>(sh.ptr + C::kOffML);  // [4][RB][2]
   if (warp < 4) {  // only warps 0-3 take blocks (4 per tile); 4-7 help write rows
 #pragma unroll
