@@ -27,6 +27,10 @@ struct MergeItem {
   int32_t tok, poff, count, pad;
 };
 
+// CTAs whose unit ranges travel in the launch parameters (read from the
+// constant bank at start-up instead of a dependent global load).
+constexpr int kInlineCtas = 320;
+
 struct AttnParams {
   const UnitDesc* units;
   const int2* blocks;        // {page, span_pos * 32 + valid}
@@ -50,6 +54,9 @@ struct AttnParams {
   int32_t* merge_cnt;
   const int32_t* tok_poff;
   int32_t merge_fused;
+  // grid <= kInlineCtas: cta_off copied here, cta_inline = 1
+  int32_t cta_inline;
+  int32_t cta_off_inline[kInlineCtas + 1];
 };
 
 struct MergeParams {

@@ -287,6 +287,9 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
   ap.merge_cnt = P->d_merge_cnt;
   ap.tok_poff = P->d_tok_poff;
   ap.merge_fused = h.opt.merge_mode == 1 ? 1 : 0;
+  ap.cta_inline = h.grid <= ta::kInlineCtas ? 1 : 0;
+  if (ap.cta_inline)
+    for (int c = 0; c <= h.grid; ++c) ap.cta_off_inline[c] = h.cta_off[c];
   cudaError_t e;
   if (P->profiling) {
     e = cudaEventRecord(P->ev[0], s);

@@ -197,6 +197,9 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   ap.merge_cnt = reinterpret_cast<int32_t*>(base + o_cnt);
   ap.tok_poff = reinterpret_cast<const int32_t*>(base + o_poff);
   ap.merge_fused = h.opt.merge_mode == 1 ? 1 : 0;
+  ap.cta_inline = h.grid <= ta::kInlineCtas ? 1 : 0;
+  if (ap.cta_inline)
+    for (int c = 0; c <= h.grid; ++c) ap.cta_off_inline[c] = h.cta_off[c];
   e = launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
   if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("partial attention launch: ") + cudaGetErrorString(e));
   if (nmerge && !ap.merge_fused) {

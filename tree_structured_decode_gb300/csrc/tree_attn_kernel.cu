@@ -1022,7 +1022,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   sh.tmem_slot = reinterpret_cast<volatile uint32_t*>(sh.ptr + C::kOffBar + C::kNumBars * 8);
   sh.abort_flag = reinterpret_cast<volatile int*>(sh.ptr + C::kOffBar + C::kNumBars * 8 + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u0 = p.cta_off[blockIdx.x], u1 = p.cta_off[blockIdx.x + 1];
+  const int u0 = p.cta_inline ? p.cta_off_inline[blockIdx.x] : p.cta_off[blockIdx.x];
+  const int u1 = p.cta_inline ? p.cta_off_inline[blockIdx.x + 1] : p.cta_off[blockIdx.x + 1];
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
