@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int total = p.n_items * p.hq;
+  // launched as a programmatic dependent of the partial-attention kernel:
+  // wait here until that grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int r0 = 2 * gw; r0 < total; r0 += 2 * nw) {
     const int idx = r0 + sub;
     if (idx >= total) continue;
@@ -136,24 +139,29 @@ cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
   const long long warps = ((long long)p.n_items * p.hq + 1) / 2;  // two rows per warp
   const int blocks = (int)((warps + 7) / 8 < 152 * 16 ? (warps + 7) / 8 : 152 * 16);
+  // A programmatic dependent launch: the merge grid may be scheduled while
+  // the partial-attention kernel finishes (it waits in griddepcontrol.wait
+  // for that grid's completion), so its launch latency leaves the step.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   // one round of loads per token where possible; fewer partials per round
   // leave registers for more resident warps
   if (d == 128) {
-    if (p.max_count > 8)
-      lse_merge_kernel<128, 24, 1><<<blocks, 256, 0, s>>>(p);
-    else if (p.max_count > 4)
-      lse_merge_kernel<128, 8, 3><<<blocks, 256, 0, s>>>(p);
-    else
-      lse_merge_kernel<128, 4, 5><<<blocks, 256, 0, s>>>(p);
-  } else {
-    if (p.max_count > 8)
-      lse_merge_kernel<64, 24, 1><<<blocks, 256, 0, s>>>(p);
-    else if (p.max_count > 4)
-      lse_merge_kernel<64, 8, 3><<<blocks, 256, 0, s>>>(p);
-    else
-      lse_merge_kernel<64, 4, 6><<<blocks, 256, 0, s>>>(p);
+    if (p.max_count > 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 24, 1>, p);
+    if (p.max_count > 4) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 8, 3>, p);
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 4, 5>, p);
   }
-  return cudaGetLastError();
+  if (p.max_count > 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<64, 24, 1>, p);
+  if (p.max_count > 4) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<64, 8, 3>, p);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<64, 4, 6>, p);
 }
 
 }  // namespace ta

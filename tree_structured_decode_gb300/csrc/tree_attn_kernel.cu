@@ -1022,6 +1022,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   sh.tmem_slot = reinterpret_cast<volatile uint32_t*>(sh.ptr + C::kOffBar + C::kNumBars * 8);
   sh.abort_flag = reinterpret_cast<volatile int*>(sh.ptr + C::kOffBar + C::kNumBars * 8 + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the merge kernel (a programmatic dependent) may be scheduled from now on;
+  // it waits for this grid's completion before reading any partial
+  asm volatile("griddepcontrol.launch_dependents;");
   const int u0 = p.cta_inline ? p.cta_off_inline[blockIdx.x] : p.cta_off[blockIdx.x];
   const int u1 = p.cta_inline ? p.cta_off_inline[blockIdx.x + 1] : p.cta_off[blockIdx.x + 1];
 
