@@ -330,7 +330,7 @@ def bench_ours(args, rank, world, local):
         "device_status": code,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec, q, k, v, work, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(spec, q, k, v, work, args.cpu_seconds, args.workload)
     return line
 
 
@@ -368,10 +368,35 @@ def _oracle_sample(spec, q, k, v, budget_s):
     return full_s, note, cores
 
 
-def cpu_baseline(spec, q, k, v, work, budget_s):
+_ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                   "BLIS_NUM_THREADS", "NUMEXPR_NUM_THREADS")
+
+
+def _single_core_sample(workload, budget_s):
+    """The oracle's seconds per full step on one core: a child process with
+    every BLAS / OpenMP pool set to one thread (set before numpy loads)."""
+    env = dict(os.environ)
+    for name in _ONE_THREAD_ENV:
+        env[name] = "1"
+    cmd = [sys.executable, os.path.abspath(__file__), "--single-core-sample", workload,
+           "--cpu-seconds", str(budget_s)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s * 4 + 120)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+    except (subprocess.TimeoutExpired, ValueError, IndexError):
+        return None
+
+
+def cpu_baseline(spec, q, k, v, work, budget_s, workload):
     full_s, note, cores = _oracle_sample(spec, q, k, v, budget_s)
-    return {"value": round(work["bytes"] / full_s / 1e9, 4), "unit": "GB/s", "cores": cores,
-            "kind": "oracle", "sample": note, "ms_per_step": round(full_s * 1e3, 2)}
+    line = {"value": round(work["bytes"] / full_s / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "cores_available": len(os.sched_getaffinity(0)), "kind": "oracle", "sample": note,
+            "ms_per_step": round(full_s * 1e3, 2)}
+    one = _single_core_sample(workload, max(2.0, budget_s / 3))
+    if one:
+        line["single_core"] = {"value": round(work["bytes"] / one["full_s"] / 1e9, 4), "unit": "GB/s",
+                               "ms_per_step": round(one["full_s"] * 1e3, 2), "sample": one["note"]}
+    return line
 
 
 def bench_reference(args, rank, world):
@@ -414,6 +439,7 @@ def main():
     ap.add_argument("--workload", default="long", choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single-core-sample", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--edges", default="greedy", choices=["greedy", "zero", "one"],
                     help="edge assignment: the greedy algorithm, or every edge 0 / 1 (ablation)")
     ap.add_argument("--plan", action="append", default=[], metavar="KEY=VALUE",
@@ -424,6 +450,15 @@ def main():
         k, _, v = kv.partition("=")
         args.plan_opts[k] = int(v)
     args.warmup = max(3, args.warmup)
+    if args.single_core_sample:  # child of cpu_baseline(): one thread everywhere
+        import torch
+
+        torch.set_num_threads(1)
+        spec = W.CONFIGS[args.single_core_sample]()
+        q, k, v = W.make_tensors(spec, device="cpu")
+        full_s, note, _ = _oracle_sample(spec, q, k, v, args.cpu_seconds)
+        print(json.dumps({"full_s": full_s, "note": note}))
+        return
     rank, world, local = dist_env()
     if args.impl == "reference":
         if world > 1 and rank != 0:
