@@ -82,8 +82,11 @@ typedef struct {
                                (thin groups are packed four to a tile)      */
   int32_t split_tokens;     /* [0 = automatic] chunk length for splitting
                                long spans; < 0 disables splitting            */
-  int32_t min_split_tokens; /* [256] smallest automatic chunk               */
-  int32_t split_waves;      /* [2] automatic split aims at waves x SMs units */
+  int32_t min_split_tokens; /* [256] smallest automatic chunk (half of it
+                               for thin groups packed by kv head)           */
+  int32_t split_waves;      /* [2] automatic split aims at waves x SMs units
+                               (thin groups packed by kv head: one unit per
+                               CTA, two CTAs per SM)                         */
   int32_t num_sms;          /* [0 = the current device's, else 152]          */
   int32_t force_path;       /* [0 = by rows] 1 = CUDA cores, 2 = tensor cores */
   int32_t host_only;        /* [0] 1: plan on the host only (describe/stats),
