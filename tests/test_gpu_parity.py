@@ -220,3 +220,34 @@ def test_draft_token_tree_verification(hq, hkv):
     out, lse, _ = run_gpu(spec, q, k, v)
     ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
     compare(out, lse, ref, ref_lse)
+
+
+# ----------------------------------------------------------------- grid size
+def test_grid_larger_than_the_inline_unit_ranges():
+    # more CTAs than the launch parameters carry unit ranges for (320): every
+    # CTA reads its range from the table in global memory; the grid also
+    # exceeds what is resident at once (two CTAs on each of the 152 SMs)
+    spec = W.config_wide()
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, stats = run_gpu(spec, q, k, v, num_sms=200)
+    assert stats["grid"] > 320
+    toks = sample_tokens(spec, 24, seed=3)
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
+    compare(out, lse, ref, ref_lse, toks)
+
+
+@pytest.mark.parametrize("num_sms", [8, 37, 152])
+def test_kv_head_packed_chunks_at_any_page(num_sms):
+    # thin groups packed by kv head split into near-equal chunks whose
+    # boundaries need not fall on a 4-page tile: the number of SMs the plan
+    # assumes moves them (it sets the chunk length)
+    rng = np.random.default_rng(num_sms)
+    lens = [int(x) for x in rng.integers(150, 900, size=5)]
+    parent = [-1, 0, 0, 1, 1]
+    qnode = [2, 2, 3, 4, 4]
+    qend = [lens[2], lens[2] - 1, lens[3], lens[4], lens[4] - 1]
+    spec = W._finish("chunks", parent, lens, qnode, qend, 16, 8, 128, seed=num_sms)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, stats = run_gpu(spec, q, k, v, num_sms=num_sms)
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    compare(out, lse, ref, ref_lse)
