@@ -251,3 +251,28 @@ def test_kv_head_packed_chunks_at_any_page(num_sms):
     out, lse, stats = run_gpu(spec, q, k, v, num_sms=num_sms)
     ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
     compare(out, lse, ref, ref_lse)
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 4), (16, 4), (64, 4)])
+def test_two_round_packed_units(hq, hkv):
+    # short leaves under one root: those of at most 16 rows per kv head pack
+    # eight to a unit in two rounds (round 0 in lanes 0-15 of each warp, round
+    # 1 in lanes 16-31; the tiles carry round 0's pages, then round 1's),
+    # longer ones four to a unit; page counts differ inside a round
+    rng = np.random.default_rng(hq)
+    nleaf = 27
+    lens = [200] + [int(x) for x in rng.integers(1, 129, size=nleaf)]
+    ntok = [1 + (v % 3 == 0) * int(rng.integers(1, 4)) for v in range(1, nleaf + 1)]
+    qnode = [v for v in range(1, nleaf + 1) for _ in range(ntok[v - 1])]
+    qend = [max(0, lens[v] - j) for v in range(1, nleaf + 1) for j in range(ntok[v - 1])]
+    spec = W._finish("rounds", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=hq)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    units = {}
+    # planned for one SM: two rounds need three units per CTA, which a tree
+    # this small has only for a grid of two CTAs
+    for name, opts in (("rounds", {"num_sms": 1}), ("one round", {}), ("unpacked", {"no_pack": 1})):
+        out, lse, stats = run_gpu(spec, q, k, v, **opts)
+        compare(out, lse, ref, ref_lse)
+        units[name] = stats["n_units"]
+    assert units["rounds"] < units["one round"] < units["unpacked"]

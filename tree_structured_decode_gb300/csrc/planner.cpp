@@ -387,10 +387,14 @@ tree_attn_status build_host_plan(
     // balance worse than the per-unit overhead they save)
     return -1;
   };
-  std::vector<int32_t> pack_mma, pack_simt;  // group indices, in group order
+  // tensor-core groups of at most half a slot pack two rounds to a unit
+  auto half_slot = [&](const GroupInfo& g) {
+    return g.rows <= kPackMmaRows / 2 && (kPackMmaRows / 2) % r == 0;
+  };
+  std::vector<int32_t> pack_mma, pack_mma2, pack_simt;  // group indices, in group order
   for (size_t gi = 0; gi < p.groups.size(); ++gi) {
     const int k = packable(p.groups[gi]);
-    if (k == kPathMma) pack_mma.push_back((int32_t)gi);
+    if (k == kPathMma) (half_slot(p.groups[gi]) ? pack_mma2 : pack_mma).push_back((int32_t)gi);
     if (k == kPathSimt) pack_simt.push_back((int32_t)gi);
   }
   // Longer thin tensor-core groups are packed by kv head: four kv heads of
@@ -417,43 +421,57 @@ tree_attn_status build_host_plan(
   // Packed units: row records laid out slot by slot (slot_rows rows per
   // slot; filler records have tok -1), and an interleaved block list
   // (tile j = page j of each slot's group, zero-valid filler pages past a
-  // group's end or for an empty slot).  Records and blocks do not depend on
-  // the kv head, so all kv heads share them.
-  auto emit_packs = [&](const std::vector<int32_t>& list, int path) {
+  // group's end or for an empty slot).  In two rounds, a slot's rows are
+  // round 0's group then round 1's (half a slot each) and the tiles carry
+  // round 0's pages, then round 1's, each page record marked with its
+  // round.  Records and blocks do not depend on the kv head, so all kv
+  // heads share them.
+  auto emit_packs = [&](const std::vector<int32_t>& list, int path, int rounds) {
     const int slot_rows = path == kPathMma ? kPackMmaRows : kPackSimtRows;
-    for (size_t s0 = 0; s0 < list.size(); s0 += kPackSlots) {
-      const size_t ns = std::min<size_t>(kPackSlots, list.size() - s0);
+    const int round_rows = slot_rows / rounds;
+    const size_t per_unit = (size_t)kPackSlots * rounds;
+    for (size_t s0 = 0; s0 < list.size(); s0 += per_unit) {
+      const size_t ns = std::min<size_t>(per_unit, list.size() - s0);
+      auto grp = [&](int rho, int k) -> const GroupInfo* {
+        const size_t i = (size_t)rho * kPackSlots + k;
+        return i < ns ? &p.groups[list[s0 + i]] : nullptr;
+      };
       const int32_t tok_off = (int32_t)p.gtok.size();
-      for (int k = 0; k < kPackSlots; ++k) {
-        const GroupInfo* g = (size_t)k < ns ? &p.groups[list[s0 + k]] : nullptr;
-        for (int e = 0; e < slot_rows / r; ++e) {
-          if (g && e < g->ntok) {
-            p.gtok.push_back(p.gtok[g->tok_off + e]);
-            p.gvis.push_back(p.gvis[g->tok_off + e]);
-            p.gpbase.push_back(p.gpbase[g->tok_off + e]);
-          } else {
-            p.gtok.push_back(-1);
-            p.gvis.push_back(0);
-            p.gpbase.push_back(-1);
+      for (int k = 0; k < kPackSlots; ++k)
+        for (int rho = 0; rho < rounds; ++rho) {
+          const GroupInfo* g = grp(rho, k);
+          for (int e = 0; e < round_rows / r; ++e) {
+            if (g && e < g->ntok) {
+              p.gtok.push_back(p.gtok[g->tok_off + e]);
+              p.gvis.push_back(p.gvis[g->tok_off + e]);
+              p.gpbase.push_back(p.gpbase[g->tok_off + e]);
+            } else {
+              p.gtok.push_back(-1);
+              p.gvis.push_back(0);
+              p.gpbase.push_back(-1);
+            }
+            p.gslot.push_back(k);
           }
-          p.gslot.push_back(k);
         }
-      }
-      int tiles = 0;
-      for (size_t k = 0; k < ns; ++k) tiles = std::max(tiles, p.groups[list[s0 + k]].nblk);
       const int32_t blk0 = (int32_t)p.blk_page.size();
       const int32_t filler_page = p.blk_page[p.groups[list[s0]].blk_off];
-      for (int t = 0; t < tiles; ++t)
-        for (int k = 0; k < kPackSlots; ++k) {
-          const GroupInfo* g = (size_t)k < ns ? &p.groups[list[s0 + k]] : nullptr;
-          if (g && t < g->nblk) {
-            p.blk_page.push_back(p.blk_page[g->blk_off + t]);
-            p.blk_meta.push_back(p.blk_meta[g->blk_off + t]);
-          } else {
-            p.blk_page.push_back(filler_page);
-            p.blk_meta.push_back(0);
+      for (int rho = 0; rho < rounds; ++rho) {
+        const int32_t mark = rounds > 1 ? (int32_t)rho << kRoundShift : 0;
+        int tiles = 0;
+        for (int k = 0; k < kPackSlots; ++k)
+          if (const GroupInfo* g = grp(rho, k)) tiles = std::max(tiles, g->nblk);
+        for (int t = 0; t < tiles; ++t)
+          for (int k = 0; k < kPackSlots; ++k) {
+            const GroupInfo* g = grp(rho, k);
+            if (g && t < g->nblk) {
+              p.blk_page.push_back(p.blk_page[g->blk_off + t]);
+              p.blk_meta.push_back(p.blk_meta[g->blk_off + t] | mark);
+            } else {
+              p.blk_page.push_back(filler_page);
+              p.blk_meta.push_back(mark);
+            }
           }
-        }
+      }
       const int32_t blk1 = (int32_t)p.blk_page.size();
       for (int kvh = 0; kvh < hkv; ++kvh) {
         UnitDesc u;
@@ -464,13 +482,28 @@ tree_attn_status build_host_plan(
         u.blk0 = blk0;
         u.blk1 = blk1;
         u.chunk = 0;
-        u.path = path;
+        u.path = path | (rounds > 1 ? kUnitRounds : 0);
         p.units.push_back(u);
       }
     }
   };
-  emit_packs(pack_mma, kPathMma);
-  emit_packs(pack_simt, kPathSimt);
+  // Two rounds halve the units of the short groups; they pay only while the
+  // plan keeps enough units to balance the CTAs (at least three per CTA),
+  // else the half-slot groups pack one round, four to a unit, as the others.
+  {
+    const int64_t others = (int64_t)p.units.size() +
+                           hkv * (ceil_div((int64_t)pack_mma.size(), kPackSlots) +
+                                  ceil_div((int64_t)pack_simt.size(), kPackSlots));
+    const int64_t with_rounds = others + hkv * ceil_div((int64_t)pack_mma2.size(), 2 * kPackSlots);
+    if (with_rounds < (int64_t)kRoundsMinUnitsPerCta * std::max(1, opt.num_sms) * kCtasPerSm) {
+      pack_mma.insert(pack_mma.end(), pack_mma2.begin(), pack_mma2.end());
+      std::sort(pack_mma.begin(), pack_mma.end());
+      pack_mma2.clear();
+    }
+  }
+  emit_packs(pack_mma2, kPathMma, 2);
+  emit_packs(pack_mma, kPathMma, 1);
+  emit_packs(pack_simt, kPathSimt, 1);
   for (size_t gi = 0; gi < p.groups.size(); ++gi) {
     const GroupInfo& g = p.groups[gi];
     if (!head_thin(g)) continue;
