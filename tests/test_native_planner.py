@@ -127,3 +127,20 @@ def test_draft_token_trees_match_reference(depth, branching, hq, hkv):
     spec = W.token_tree(500, 4, 90, depth, branching, hq, hkv, 128, seed=depth)
     for opt in ({}, {"split_tokens": 128}, {"gamma": 2000}):
         _same(spec, **opt)
+
+
+@pytest.mark.parametrize("num_sms", [1, 2, 5, 152])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (32, 4), (64, 4)])
+def test_two_round_packing_matches_reference(hq, hkv, num_sms):
+    # short leaves with 1-3 query tokens: groups of at most 16 rows per kv
+    # head pack eight to a unit in two rounds while the plan keeps three
+    # units per CTA (few SMs), else four to a unit like the longer ones
+    rng = np.random.default_rng(hq * 7 + num_sms)
+    nleaf = 40
+    lens = [300] + [int(x) for x in rng.integers(1, 129, size=nleaf)]
+    ntok = [int(rng.integers(1, 4)) for _ in range(nleaf)]
+    qnode = [v for v in range(1, nleaf + 1) for _ in range(ntok[v - 1])]
+    qend = [max(0, lens[v] - j) for v in range(1, nleaf + 1) for j in range(ntok[v - 1])]
+    spec = W._finish("rounds", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=hq)
+    _same(spec, num_sms=num_sms)
+    _same(spec, num_sms=num_sms, no_pack=1)
