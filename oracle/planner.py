@@ -310,16 +310,16 @@ def build_plan(parent, node_kv_len, node_page_offsets, node_pages, page_size,
         else:
             n_units += n_kv_heads * g["qtiles"] * len(g["chunks"])
     # Tensor-core groups of at most half a slot (16 rows, the GQA ratio
-    # dividing 16) pack in two rounds, eight to a unit, two per slot, when
+    # dividing 16) pack in two phases, eight to a unit, two per slot, when
     # the plan then still has at least three units per CTA (two CTAs per
     # SM); else four to a unit like the others.
     half = [k == "mma" and g["rows"] <= 16 and 16 % r == 0 for g, k in zip(groups, kinds)]
     n_full = sum(1 for k, h in zip(kinds, half) if k == "mma" and not h)
     n_simt = sum(1 for k in kinds if k == "simt")
     others = n_units + n_kv_heads * (_ceil(n_full, 4) + _ceil(n_simt, 4))
-    with_rounds = others + n_kv_heads * _ceil(sum(half), 8)
-    if with_rounds >= 3 * o.num_sms * 2:
-        n_units = with_rounds
+    with_phases = others + n_kv_heads * _ceil(sum(half), 8)
+    if with_phases >= 3 * o.num_sms * 2:
+        n_units = with_phases
     else:
         n_units = n_units + n_kv_heads * (_ceil(n_full + sum(half), 4) + _ceil(n_simt, 4))
     return {

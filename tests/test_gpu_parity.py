@@ -200,7 +200,7 @@ def test_largest_gqa_ratio():
 
 def test_tokens_with_more_partials_than_one_merge_round():
     # a 2000-token root split into 64-token chunks: every token folds 32 or
-    # more partials (two rounds of the wide merge)
+    # more partials (two phases of the wide merge)
     spec = W.two_level(2000, 3, 50, 8, 2, 128, seed=9)
     q, k, v = make_inputs(spec, tail_fill=float("nan"))
     out, lse, stats = run_gpu(spec, q, k, v, split_tokens=64)
@@ -254,25 +254,25 @@ def test_kv_head_packed_chunks_at_any_page(num_sms):
 
 
 @pytest.mark.parametrize("hq,hkv", [(32, 4), (16, 4), (64, 4)])
-def test_two_round_packed_units(hq, hkv):
+def test_two_phase_packed_units(hq, hkv):
     # short leaves under one root: those of at most 16 rows per kv head pack
-    # eight to a unit in two rounds (round 0 in lanes 0-15 of each warp, round
-    # 1 in lanes 16-31; the tiles carry round 0's pages, then round 1's),
-    # longer ones four to a unit; page counts differ inside a round
+    # eight to a unit in two phases (phase 0 in lanes 0-15 of each warp,
+    # phase 1 in lanes 16-31; the tiles carry phase 0's pages, then phase
+    # 1's), longer ones four to a unit; page counts differ inside a phase
     rng = np.random.default_rng(hq)
     nleaf = 27
     lens = [200] + [int(x) for x in rng.integers(1, 129, size=nleaf)]
     ntok = [1 + (v % 3 == 0) * int(rng.integers(1, 4)) for v in range(1, nleaf + 1)]
     qnode = [v for v in range(1, nleaf + 1) for _ in range(ntok[v - 1])]
     qend = [max(0, lens[v] - j) for v in range(1, nleaf + 1) for j in range(ntok[v - 1])]
-    spec = W._finish("rounds", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=hq)
+    spec = W._finish("phases", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=hq)
     q, k, v = make_inputs(spec, tail_fill=float("nan"))
     ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
     units = {}
-    # planned for one SM: two rounds need three units per CTA, which a tree
+    # planned for one SM: two phases need three units per CTA, which a tree
     # this small has only for a grid of two CTAs
-    for name, opts in (("rounds", {"num_sms": 1}), ("one round", {}), ("unpacked", {"no_pack": 1})):
+    for name, opts in (("phases", {"num_sms": 1}), ("one phase", {}), ("unpacked", {"no_pack": 1})):
         out, lse, stats = run_gpu(spec, q, k, v, **opts)
         compare(out, lse, ref, ref_lse)
         units[name] = stats["n_units"]
-    assert units["rounds"] < units["one round"] < units["unpacked"]
+    assert units["phases"] < units["one phase"] < units["unpacked"]

@@ -131,9 +131,9 @@ def test_draft_token_trees_match_reference(depth, branching, hq, hkv):
 
 @pytest.mark.parametrize("num_sms", [1, 2, 5, 152])
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (32, 4), (64, 4)])
-def test_two_round_packing_matches_reference(hq, hkv, num_sms):
+def test_two_phase_packing_matches_reference(hq, hkv, num_sms):
     # short leaves with 1-3 query tokens: groups of at most 16 rows per kv
-    # head pack eight to a unit in two rounds while the plan keeps three
+    # head pack eight to a unit in two phases while the plan keeps three
     # units per CTA (few SMs), else four to a unit like the longer ones
     rng = np.random.default_rng(hq * 7 + num_sms)
     nleaf = 40
@@ -141,6 +141,6 @@ def test_two_round_packing_matches_reference(hq, hkv, num_sms):
     ntok = [int(rng.integers(1, 4)) for _ in range(nleaf)]
     qnode = [v for v in range(1, nleaf + 1) for _ in range(ntok[v - 1])]
     qend = [max(0, lens[v] - j) for v in range(1, nleaf + 1) for j in range(ntok[v - 1])]
-    spec = W._finish("rounds", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=hq)
+    spec = W._finish("phases", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=hq)
     _same(spec, num_sms=num_sms)
     _same(spec, num_sms=num_sms, no_pack=1)

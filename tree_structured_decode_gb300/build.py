@@ -3,7 +3,8 @@
     python -m tree_structured_decode_gb300.build
 
 Translation units compile in parallel; the shared library links the CUDA
-runtime statically, so it needs only the driver at run time.  Output:
+runtime statically, so it needs only the CUDA driver library (libcuda) at
+run time.  Output:
 ``tree_structured_decode_gb300/lib/libtreeattn.so``.
 """
 from __future__ import annotations

@@ -387,7 +387,7 @@ tree_attn_status build_host_plan(
     // balance worse than the per-unit overhead they save)
     return -1;
   };
-  // tensor-core groups of at most half a slot pack two rounds to a unit
+  // tensor-core groups of at most half a slot pack two phases to a unit
   auto half_slot = [&](const GroupInfo& g) {
     return g.rows <= kPackMmaRows / 2 && (kPackMmaRows / 2) % r == 0;
   };
@@ -421,15 +421,15 @@ tree_attn_status build_host_plan(
   // Packed units: row records laid out slot by slot (slot_rows rows per
   // slot; filler records have tok -1), and an interleaved block list
   // (tile j = page j of each slot's group, zero-valid filler pages past a
-  // group's end or for an empty slot).  In two rounds, a slot's rows are
-  // round 0's group then round 1's (half a slot each) and the tiles carry
-  // round 0's pages, then round 1's, each page record marked with its
-  // round.  Records and blocks do not depend on the kv head, so all kv
+  // group's end or for an empty slot).  In two phases, a slot's rows are
+  // phase 0's group then phase 1's (half a slot each) and the tiles carry
+  // phase 0's pages, then phase 1's, each page record marked with its
+  // phase.  Records and blocks do not depend on the kv head, so all kv
   // heads share them.
-  auto emit_packs = [&](const std::vector<int32_t>& list, int path, int rounds) {
+  auto emit_packs = [&](const std::vector<int32_t>& list, int path, int phases) {
     const int slot_rows = path == kPathMma ? kPackMmaRows : kPackSimtRows;
-    const int round_rows = slot_rows / rounds;
-    const size_t per_unit = (size_t)kPackSlots * rounds;
+    const int phase_rows = slot_rows / phases;
+    const size_t per_unit = (size_t)kPackSlots * phases;
     for (size_t s0 = 0; s0 < list.size(); s0 += per_unit) {
       const size_t ns = std::min<size_t>(per_unit, list.size() - s0);
       auto grp = [&](int rho, int k) -> const GroupInfo* {
@@ -438,9 +438,9 @@ tree_attn_status build_host_plan(
       };
       const int32_t tok_off = (int32_t)p.gtok.size();
       for (int k = 0; k < kPackSlots; ++k)
-        for (int rho = 0; rho < rounds; ++rho) {
+        for (int rho = 0; rho < phases; ++rho) {
           const GroupInfo* g = grp(rho, k);
-          for (int e = 0; e < round_rows / r; ++e) {
+          for (int e = 0; e < phase_rows / r; ++e) {
             if (g && e < g->ntok) {
               p.gtok.push_back(p.gtok[g->tok_off + e]);
               p.gvis.push_back(p.gvis[g->tok_off + e]);
@@ -455,8 +455,8 @@ tree_attn_status build_host_plan(
         }
       const int32_t blk0 = (int32_t)p.blk_page.size();
       const int32_t filler_page = p.blk_page[p.groups[list[s0]].blk_off];
-      for (int rho = 0; rho < rounds; ++rho) {
-        const int32_t mark = rounds > 1 ? (int32_t)rho << kRoundShift : 0;
+      for (int rho = 0; rho < phases; ++rho) {
+        const int32_t mark = phases > 1 ? (int32_t)rho << kPhaseShift : 0;
         int tiles = 0;
         for (int k = 0; k < kPackSlots; ++k)
           if (const GroupInfo* g = grp(rho, k)) tiles = std::max(tiles, g->nblk);
@@ -482,20 +482,20 @@ tree_attn_status build_host_plan(
         u.blk0 = blk0;
         u.blk1 = blk1;
         u.chunk = 0;
-        u.path = path | (rounds > 1 ? kUnitRounds : 0);
+        u.path = path | (phases > 1 ? kUnitPhases : 0);
         p.units.push_back(u);
       }
     }
   };
-  // Two rounds halve the units of the short groups; they pay only while the
+  // Two phases halve the units of the short groups; they pay only while the
   // plan keeps enough units to balance the CTAs (at least three per CTA),
-  // else the half-slot groups pack one round, four to a unit, as the others.
+  // else the half-slot groups pack one phase, four to a unit, as the others.
   {
     const int64_t others = (int64_t)p.units.size() +
                            hkv * (ceil_div((int64_t)pack_mma.size(), kPackSlots) +
                                   ceil_div((int64_t)pack_simt.size(), kPackSlots));
-    const int64_t with_rounds = others + hkv * ceil_div((int64_t)pack_mma2.size(), 2 * kPackSlots);
-    if (with_rounds < (int64_t)kRoundsMinUnitsPerCta * std::max(1, opt.num_sms) * kCtasPerSm) {
+    const int64_t with_phases = others + hkv * ceil_div((int64_t)pack_mma2.size(), 2 * kPackSlots);
+    if (with_phases < (int64_t)kPhasesMinUnitsPerCta * std::max(1, opt.num_sms) * kCtasPerSm) {
       pack_mma.insert(pack_mma.end(), pack_mma2.begin(), pack_mma2.end());
       std::sort(pack_mma.begin(), pack_mma.end());
       pack_mma2.clear();

@@ -34,13 +34,13 @@ static_assert(kPackSlots == kBlocksPerTile, "one page per slot per tile");
 constexpr int kPathSimt = 0;
 constexpr int kPathMma = 1;
 constexpr int kUnitHeads = 2;  // with kPathMma: slot k of the unit is kv head kvh + k
-// with kPathMma: a packed unit in two rounds; each slot (warp) holds two
-// groups of at most 16 rows, round 0's in lanes 0-15 and round 1's in lanes
-// 16-31, and the unit's tiles carry round 0's pages, then round 1's
-constexpr int kUnitRounds = 4;
-constexpr int kRoundsMinUnitsPerCta = 3;         // two rounds only with this many units per CTA
-constexpr int kRoundShift = 30;                  // round of a packed tile's page record
-constexpr int32_t kPosMask = (1 << kRoundShift) - 1;
+// with kPathMma: a packed unit in two phases; each slot (warp) holds two
+// groups of at most 16 rows, phase 0's in lanes 0-15 and phase 1's in lanes
+// 16-31, and the unit's tiles carry phase 0's pages, then phase 1's
+constexpr int kUnitPhases = 4;
+constexpr int kPhasesMinUnitsPerCta = 3;         // two phases only with this many units per CTA
+constexpr int kPhaseShift = 30;                  // phase of a packed tile's page record
+constexpr int32_t kPosMask = (1 << kPhaseShift) - 1;
 
 struct Options {
   int64_t gamma = 64;

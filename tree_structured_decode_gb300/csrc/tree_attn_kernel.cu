@@ -810,11 +810,11 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         }
         full = full && (!row_ok || lim[bb] == 16);
       }
-      // in a unit packed in two rounds a row sees only its round's tiles
-      // (round 0 in lanes 0-15, round 1 in lanes 16-31 of each slot)
-      const bool my_round =
-          !(u.path & kUnitRounds) || ((mt_p >> kRoundShift) & 1) == ((tid & 31) >> 4);
-      const int lim_p = packed && row_ok && my_round
+      // in a unit packed in two phases a row sees only its phase's tiles
+      // (phase 0 in lanes 0-15, phase 1 in lanes 16-31 of each slot)
+      const bool my_phase =
+          !(u.path & kUnitPhases) || ((mt_p >> kPhaseShift) & 1) == ((tid & 31) >> 4);
+      const int lim_p = packed && row_ok && my_phase
                             ? max(0, min(mt_p & 31, vis - ((mt_p & kPosMask) >> 5)))
                             : 0;
       int nvalid = 0;  // valid slots of the tile's pages, 5 bits each
