@@ -1,4 +1,5 @@
 import os
+import shutil
 import sys
 
 import pytest
@@ -10,6 +11,17 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a)")
+
+
+def pytest_sessionstart(session):
+    # A fresh checkout has no library yet: build it (nvcc cross-compiles
+    # without a GPU).  The tests then load the real library; without nvcc the
+    # library tests fail loudly, as the product does (no fallback).
+    lib = os.path.join(ROOT, "tree_structured_decode_gb300", "lib", "libtreeattn.so")
+    if not os.path.exists(lib) and shutil.which("nvcc"):
+        from tree_structured_decode_gb300 import build
+
+        build.build()
 
 
 def pytest_collection_modifyitems(config, items):
