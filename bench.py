@@ -8,10 +8,13 @@ One step = one tree_attn_run() of the workload (the partial-attention pass and
 the log-sum-exp merge, one layer), inputs resident in HBM, L2 flushed before
 every step outside the step's events: a 512 MiB memset, then a 256 MiB read,
 so that the step starts from clean L2 lines (after the memset alone, the
-step's cold reads would also pay for writing back the memset's dirty lines).  The workload is the
-long-context tail tree with the Llama-2-7B attention shape (32 q heads = 32 kv
-heads, d = 128, one layer): root 4000 tokens, 10 leaves of 400, one decode
-query per leaf, bf16 N(0, 1) Q/K/V in 16-token pages in shuffled order.
+step's cold reads would also pay for writing back the memset's dirty lines).
+The default workload is the largest of the five synthetic trees: the
+irregular random tree (depth 4-5, branching 1-8, node lengths log-uniform in
+16-2048, ~1000 leaves each carrying 4 speculative query tokens with a causal
+mask over its own last 4 tokens; 64 q / 4 kv heads, d = 128), bf16 N(0, 1)
+Q/K/V in 16-token pages in shuffled order.  The other four trees are timed
+the same way (fewer steps) and reported under "per_workload".
 
 Metric: algorithmic HBM bytes per second (unique KV + Q + out + lse bytes of
 the step / device time of the step), with ms per step beside it.  Under
@@ -109,19 +112,118 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def committed_traffic(kernel_src: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if the summary was taken on the current kernel source."""
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+CSRC = os.path.join(ROOT, "tree_structured_decode_gb300", "csrc")
+
+
+def source_hash() -> str:
+    """sha256 (16 hex digits) over every source file of the library (kernels,
+    planner, runtime), in name order: a profile taken on other sources does
+    not describe the kernels this run times."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".cpp", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(CSRC, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch of the partial-attention kernel from the
+    committed ncu summary of this workload, if that summary was captured on
+    the current library sources; else None."""
     path = os.path.join(ROOT, "profiles", f"partial_attention_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_sha = re.search(r"library_source_sha256_16:\s*([0-9a-f]+)", txt)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.e+]+)", txt)
-    if m_sha and m_b and m_sha.group(1) == sha:
+    if m_sha and m_b and m_sha.group(1) == source_hash():
         return float(m_b.group(1))
     return None
+
+
+class NvmlClocks:
+    """SM clock and clock-event (throttle) reasons polled through NVML (the
+    library nvidia-smi reads) every ~2 ms on a thread while the timed steps
+    run, so that even a short timed region gets many samples."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        import ctypes
+        import threading
+
+        self.ok = False
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            got = False
+            try:
+                import torch
+                uuid = str(torch.cuda.get_device_properties(torch_device).uuid)
+                if not uuid.startswith("GPU-"):
+                    uuid = "GPU-" + uuid
+                got = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                got = False
+            if not got:
+                idx = torch_device.index or 0
+                got = lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) == 0
+            if not got:
+                return
+            self.lib, self.h = lib, h
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 \
+                else None
+            self.ctypes = ctypes
+            self.ok = True
+        except OSError:
+            return
+
+    def _poll(self):
+        c = self.ctypes
+        mhz, rs = c.c_uint(), c.c_ulonglong()
+        while not self._stop.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz)) == 0 and \
+                    self.reasons_fn(self.h, c.byref(rs)) == 0:
+                self.samples.append((float(mhz.value), int(rs.value)))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        import threading
+
+        if self.ok:
+            self._stop.clear()
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self._thread = None
+
+    def result(self):
+        if not self.samples:
+            return None
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        sm = [m for m, _ in self.samples]
+        return {"sm_mhz": float(np.median(sm)), "sm_min_mhz": float(min(sm)),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(sm), "source": "NVML, polled every ~2 ms during the timed steps"}
 
 
 class ClockSampler:
@@ -198,42 +300,22 @@ def aggregate_gbs(bytes_per_step, world, step_ms):
 
 
 # --------------------------------------------------------------------------- ours
-def bench_ours(args, rank, world, local):
+def time_steps(plan, q, k, v, out, lse, flush, stream, steps, warmup, clocks=None):
+    """Warm up, then time `steps` steps (one event pair around each whole
+    run(), L2 flushed before each outside the events); then the same steps
+    again with the library's per-kernel events (they sit between the two
+    kernels, so they stay out of the step time)."""
     import torch
 
-    import tree_structured_decode_gb300 as ta
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    spec = W.CONFIGS[args.workload]()
-    work = algorithmic_work(spec)
-    q, k, v = W.make_tensors(spec, device=dev)
-    torch.cuda.synchronize()
-    opts = dict(args.plan_opts)
-    if args.edges != "greedy":  # plan ablation: every edge 0 (no joins) or 1 (join every chain)
-        opts["force_edges"] = np.full(spec.n_nodes, 1 if args.edges == "one" else 0, dtype=np.int8)
-    plan = ta.Plan.from_spec(spec, **opts)
-    stats = plan.stats()
-    out = torch.empty((spec.n_queries, spec.n_q_heads, spec.head_dim), dtype=torch.float32,
-                      device=dev)
-    lse = torch.empty((spec.n_queries, spec.n_q_heads), dtype=torch.float32, device=dev)
-    flush = L2Flush(dev)
-    stream = torch.cuda.current_stream()
-    launches_per_step = 1 + (1 if stats["n_merge_tokens"] > 0 else 0)
-
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush()
         plan.run(q, k, v, out=out, lse=lse)
     torch.cuda.synchronize()
-    assert plan.device_status() == 0
-
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     step_ms, part_ms, merge_ms = [], [], []
-    with ClockSampler(local) as clk:
-        # the steps: one event pair around each whole run()
-        for _ in range(args.steps):
+    if clocks is not None:
+        clocks.__enter__()
+    try:
+        for _ in range(steps):
             flush()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -242,21 +324,89 @@ def bench_ours(args, rank, world, local):
             e1.record(stream)
             e1.synchronize()
             step_ms.append(e0.elapsed_time(e1))
-        # the same steps again with the library's per-kernel events (they
-        # sit between the two kernels, so they are kept out of the step time)
-        plan.profile(True)
-        for _ in range(args.steps):
-            flush()
-            plan.run(q, k, v, out=out, lse=lse)
-            a, b = plan.kernel_times()
-            part_ms.append(a)
-            merge_ms.append(b)
-        plan.profile(False)
-        torch.cuda.synchronize()
-        clocks = clk.result()
+    finally:
+        if clocks is not None:
+            clocks.__exit__()
+    plan.profile(True)
+    for _ in range(steps):
+        flush()
+        plan.run(q, k, v, out=out, lse=lse)
+        a, b = plan.kernel_times()
+        part_ms.append(a)
+        merge_ms.append(b)
+    plan.profile(False)
+    torch.cuda.synchronize()
+    return step_ms, part_ms, merge_ms
+
+
+def roofline(work, t_part, t_step, workload):
+    """The partial-attention kernel against the slower of the HBM and tensor
+    bounds of the step's algorithmic bytes and FLOPs (measured peaks)."""
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
+    t_hbm = work["bytes"] / (hbm_peak * 1e9)
+    t_tc = work["flops"] / (tc_peak * 1e12)
+    if t_hbm >= t_tc:
+        kern_gbs = work["bytes"] / (t_part * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(kern_gbs / hbm_peak, 4)}
+    else:
+        tf = work["flops"] / (t_part * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(tf / tc_peak, 4)}
+    roof["peak_source"] = peak_kind + " (burst: the kernel is timed alone)"
+    roof["traffic"] = committed_traffic(workload)
+    roof["kernel"] = "partial attention pass (tree_attn_kernel)"
+    roof["kernel_ms"] = round(t_part, 5)
+    roof["step_roofline_frac"] = round(max(t_hbm, t_tc) * 1e3 / t_step, 4)
+    return roof
+
+
+def bench_workload(name, dev, flush, stream, steps, warmup, opts, clocks=None):
+    """Plan and time one workload; returns its numbers and the live objects."""
+    import torch
+
+    import tree_structured_decode_gb300 as ta
+
+    spec = W.CONFIGS[name]()
+    work = algorithmic_work(spec)
+    q, k, v = W.make_tensors(spec, device=dev)
+    plan = ta.Plan.from_spec(spec, **opts)
+    stats = plan.stats()
+    out = torch.empty((spec.n_queries, spec.n_q_heads, spec.head_dim), dtype=torch.float32,
+                      device=dev)
+    lse = torch.empty((spec.n_queries, spec.n_q_heads), dtype=torch.float32, device=dev)
+    step_ms, part_ms, merge_ms = time_steps(plan, q, k, v, out, lse, flush, stream, steps, warmup,
+                                            clocks)
+    code = plan.device_status()
+    return {"spec": spec, "work": work, "plan": plan, "stats": stats, "q": q, "k": k, "v": v,
+            "out": out, "lse": lse, "step_ms": step_ms, "part_ms": part_ms, "merge_ms": merge_ms,
+            "device_status": code}
+
+
+def bench_ours(args, rank, world, local):
+    import torch
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    opts = dict(args.plan_opts)
+    spec0 = W.CONFIGS[args.workload]()
+    if args.edges != "greedy":  # plan ablation: every edge 0 (no joins) or 1 (join every chain)
+        opts["force_edges"] = np.full(spec0.n_nodes, 1 if args.edges == "one" else 0, dtype=np.int8)
+    del spec0
+
     if world > 1:
         torch.distributed.barrier()
-    code = plan.device_status()
+    torch.cuda.synchronize()
+    clocks = NvmlClocks(dev)
+    r = bench_workload(args.workload, dev, flush, stream, args.steps, args.warmup, opts,
+                       clocks if clocks.ok else None)
+    if world > 1:
+        torch.distributed.barrier()
+    spec, work, plan, stats = r["spec"], r["work"], r["plan"], r["stats"]
+    q, k, v, out, lse = r["q"], r["k"], r["v"], r["out"], r["lse"]
+    launches_per_step = 1 + (1 if stats["n_merge_tokens"] > 0 else 0)
 
     # ---- end to end through the public API, host buffers (pinned) both ways
     hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
@@ -281,37 +431,45 @@ def bench_ours(args, rank, world, local):
         e1.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
+    del dq, dk, dv, hq_, hk_, hv_
 
-    t_step = float(np.mean(step_ms))
-    t_part = float(np.mean(part_ms))
+    t_step = float(np.mean(r["step_ms"]))
+    t_part = float(np.mean(r["part_ms"]))
+    t_merge = float(np.mean(r["merge_ms"]))
     t_e2e = float(np.mean(e2e_ms))
     t_step, t_e2e, t_part = reduce_max_over_ranks([t_step, t_e2e, t_part], world, dev)
-    hbm_peak, tc_peak, peak_kind = measured_peaks()
     gbs = aggregate_gbs(work["bytes"], world, t_step)
-    kern_gbs = work["bytes"] / (t_part * 1e-3) / 1e9
-    t_hbm = work["bytes"] / (hbm_peak * 1e9)
-    t_tc = work["flops"] / (tc_peak * 1e12)
-    bound = "hbm" if t_hbm >= t_tc else "tensor"
-    if bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(kern_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(kern_gbs / hbm_peak, 4)}
-    else:
-        tf = work["flops"] / (t_part * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": round(tf / tc_peak, 4)}
-    roof["peak_source"] = peak_kind
-    roof["traffic"] = committed_traffic(
-        os.path.join(ROOT, "tree_structured_decode_gb300", "csrc", "tree_attn_kernel.cu"),
-        args.workload)
-    roof["kernel"] = "partial attention pass"
-    roof["kernel_ms"] = round(t_part, 5)
-    roof["merge_ms"] = round(float(np.mean(merge_ms)), 5)
-    roof["step_roofline_frac"] = round(max(t_hbm, t_tc) * 1e3 / t_step, 4)
+    roof = roofline(work, t_part, t_step, args.workload)
+    roof["merge_ms"] = round(t_merge, 5)
+
+    # ---- the other workloads, the same way (fewer steps)
+    per = {}
+    if not args.no_per_workload:
+        others = [n for n in ("tiny", "long", "wide", "three", "irreg") if n != args.workload]
+        for name in others:
+            rr = bench_workload(name, dev, flush, stream, args.per_workload_steps,
+                                min(args.warmup, 5), dict(args.plan_opts))
+            ts = float(np.mean(rr["step_ms"]))
+            tp = float(np.mean(rr["part_ms"]))
+            rf = roofline(rr["work"], tp, ts, name)
+            per[name] = {"workload": WORKLOAD_DESC[name], "steps": args.per_workload_steps,
+                         "ms_per_step": round(ts, 5),
+                         "gbs_step": round(rr["work"]["bytes"] / (ts * 1e-3) / 1e9, 1),
+                         "kernel_ms": round(tp, 5),
+                         "merge_ms": round(float(np.mean(rr["merge_ms"])), 5),
+                         "kernel_frac": rf["frac"], "bound": rf["bound"],
+                         "step_frac": rf["step_roofline_frac"], "traffic": rf["traffic"],
+                         "alg_bytes_per_step": rr["work"]["bytes"],
+                         "n_units": rr["stats"]["n_units"], "device_status": rr["device_status"]}
+            rr["plan"].close()
+            del rr
+            torch.cuda.empty_cache()
 
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step, 5),
-        "ms_per_step_p10_p50_p90": [round(float(x), 5) for x in np.percentile(step_ms, [10, 50, 90])],
+        "ms_per_step_p10_p50_p90": [round(float(x), 5)
+                                    for x in np.percentile(r["step_ms"], [10, 50, 90])],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, shuffled 16-token pages)",
         "config": {"workload": WORKLOAD_DESC[args.workload], "name": args.workload,
@@ -320,17 +478,24 @@ def bench_ours(args, rank, world, local):
                    "alg_bytes_per_step": work["bytes"], "alg_flops_per_step": work["flops"],
                    "plan": {k: stats[k] for k in ("n_groups", "n_groups_mma", "n_units", "grid",
                                                   "n_partials", "chunk_tokens", "plan_ms")},
-                   "plan_options": args.plan_opts, "edges": args.edges},
+                   "plan_options": args.plan_opts, "edges": args.edges,
+                   "library_source_sha256_16": source_hash()},
         "e2e": {"value": round(aggregate_gbs(work["bytes"], world, t_e2e), 2), "unit": "GB/s",
                 "ms_per_step": round(t_e2e, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
-        "clocks": clocks,
-        "device_status": code,
+        "clocks": clocks.result() if clocks.ok else None,
+        "device_status": r["device_status"],
+        "per_workload": per,
     }
+    if line["clocks"] is None:  # NVML unavailable: nvidia-smi over a repeat of the steps
+        with ClockSampler(local) as clk:
+            time_steps(plan, q, k, v, out, lse, flush, stream, max(args.steps, 200), 0)
+            line["clocks"] = clk.result()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, q, k, v, work, args.cpu_seconds, args.workload)
+    plan.close()
     return line
 
 
@@ -436,7 +601,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="long", choices=sorted(W.CONFIGS))
+    ap.add_argument("--workload", default="irreg", choices=sorted(W.CONFIGS))
+    ap.add_argument("--per-workload-steps", type=int, default=20)
+    ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single-core-sample", default=None, help=argparse.SUPPRESS)

@@ -37,6 +37,9 @@
  *     Slots of a page past the end of its node are never read into a result
  *     (they may hold anything, NaN included).
  *   - A query whose path holds no visible key gets out = 0, lse = -inf.
+ *   - Any finite bf16 values are valid input: partial results are kept in
+ *     fp16 divided by a per-row power of two when they would leave fp16's
+ *     range, with the divisor stored beside their log-sum-exp.
  *   - Every call returns a status; nothing is thrown across the ABI.  On
  *     failure tree_attn_last_error() describes the cause (thread-local).
  *   - Supported: head_dim in {64, 128}, page_size == 16, n_q_heads a multiple
@@ -171,8 +174,9 @@ tree_attn_status tree_attn_plan(
  * Device pointers as in the conventions above; q, k_pages, v_pages are read,
  * out (and lse if non-NULL) written in full.  One plan may be run any number
  * of times (e.g. once per layer) but by one stream at a time: its workspace
- * is shared by all runs.  Errors: TA_ERR_INVALID_ARG, TA_ERR_ALIGNMENT,
- * TA_ERR_HOST_ONLY_PLAN, TA_ERR_CUDA (launch failure). */
+ * is shared by all runs.  The current device must be the one the plan was
+ * made on.  Errors: TA_ERR_INVALID_ARG (also: another device is current),
+ * TA_ERR_ALIGNMENT, TA_ERR_HOST_ONLY_PLAN, TA_ERR_CUDA (launch failure). */
 tree_attn_status tree_attn_run(tree_attn_plan_t plan, const void* q,
                                const void* k_pages, const void* v_pages,
                                float* out, float* lse, void* stream);
@@ -210,11 +214,16 @@ tree_attn_status tree_attn_append_kv(tree_attn_plan_t plan, const void* k_new,
  * asynchrony as tree_attn_run(), and `plan` may be a host_only plan (which
  * holds no device memory), so planning and running allocate nothing on the
  * GPU.  The plan's tables and its partial results go into one static
- * scratch array of TREE_ATTN_STATIC_SCRATCH_BYTES; each call re-copies the
- * tables (stream-ordered) and clears what must start at zero.
- *   - The first call on a device looks up the scratch address on that
- *     device (the device must be current); make that first call before any
- *     stream capture.
+ * scratch array of TREE_ATTN_STATIC_SCRATCH_BYTES on the current device
+ * (whichever device the plan was made on); each call copies the plan's
+ * table image (one host-to-device copy, stream-ordered) and clears what
+ * must start at zero.
+ *   - The image sits in ordinary (pageable) host memory, so the runtime
+ *     stages that copy through its own buffer: the call returns once the
+ *     copy is staged, and is not fully asynchronous to the host.
+ *   - The first call on a device (and again after its context is made
+ *     anew) looks up the scratch address on that device; make that first
+ *     call before any stream capture.
  *   - Every call shares the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and corrupt each other's results.
  *     Serialise them, e.g. on one stream.
@@ -256,6 +265,18 @@ tree_attn_status tree_attn_profile_read(tree_attn_plan_t plan, float* partial_ms
  * full size.  Returns TA_ERR_BUFFER_TOO_SMALL if cap is too small. */
 tree_attn_status tree_attn_plan_describe(tree_attn_plan_t plan, char* buf,
                                          size_t cap, size_t* needed);
+
+/* Canonical JSON of the tables the kernels of a run read, exactly as they
+ * are copied to the device: the work units in schedule order (8 ints each:
+ * first row record, kv head, first row, rows, first block, end block,
+ * chunk, path flags), each CTA's unit range (cta_off), the blocks (page,
+ * span position * 32 + valid slots, bit 30 the phase of a two-phase unit),
+ * the row records (token, visible end, first partial slot, partial count |
+ * (slot + 1) << 24), the merge items (token, first slot, count, 0) and each
+ * token's first partial slot.  For tests and tools that check a schedule;
+ * same buffer rules as tree_attn_plan_describe(). */
+tree_attn_status tree_attn_plan_describe_schedule(tree_attn_plan_t plan, char* buf,
+                                                  size_t cap, size_t* needed);
 
 /* Copy the plan's sizes into *stats. */
 tree_attn_status tree_attn_plan_get_stats(tree_attn_plan_t plan,

@@ -10,12 +10,17 @@ Modules
              the append of the query tokens' own K/V before attention.
   planner    the greedy binary edge assignment and grouping plan, written
              from the FastTree review page (Algorithm 1 and its cost model),
-             used to check the native planner decision by decision.
+             and the chunks of the long-context split for a given chunk
+             length: the decisions the pages define, used to check the native
+             planner decision by decision.  How groups become GPU work units
+             (tiles, packing, the automatic chunk length, the CTA schedule)
+             is not the pages' and is not restated here; the tests check it
+             by invariants on the device tables.
 
 Parity status: every function here is pinned by tests that do not call it to
 check itself (closed forms, brute force, an independent tree-mask
 formulation, a library routine on special cases, the worked cases on the
-pages); none is "parity unpinned".
+pages, the cost of a plan worked out by hand); none is "parity unpinned".
 """
 from .attention import (  # noqa: F401
     node_path,
@@ -32,6 +37,7 @@ from .planner import (  # noqa: F401
     subtree_rows,
     greedy_edges,
     plan_groups,
+    split_chunks,
     build_plan,
     plan_cost,
 )

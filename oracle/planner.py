@@ -40,15 +40,9 @@ class PlannerOptions:
     ts_q_set: tuple = (16, 64, 128)      # query tile sizes (multi-stage tiling)
     ts_c: int = 64                       # context tile size
     mma_min_rows: int = 1                # rows per kv head to use tensor cores
-    mma_tile_rows: int = 128             # MMA query tile (M)
-    simt_tile_rows: int = 8              # CUDA-core query tile
+    force_path: int = 0                  # 0 by rows, 1 CUDA cores, 2 tensor cores
     kv_tile_tokens: int = 64             # chunk granularity (tokens)
-    split_tokens: int = 0                # 0 = automatic split, < 0 = never
-    min_split_tokens: int = 256          # smallest automatic chunk
-    split_waves: int = 2                 # automatic split aims at waves x SMs
-    num_sms: int = 152                   # SM count the split targets
-    force_path: int = 0                  # 0 by rows, 1 CUDA cores, 2 MMA
-    no_pack: int = 0                     # 1: never pack thin groups
+    split_tokens: int = 0                # chunk length (tokens); <= 0: no split
     edges: tuple | None = field(default=None)  # force an assignment (tests)
 
 
@@ -215,121 +209,65 @@ def _ceil(a, b):
     return -(-a // b)
 
 
+def split_chunks(n_blocks, chunk_blocks, tile_blocks):
+    """The long-context split of one group span (FastTree review page,
+    "GPU高效的长上下文分割": a span longer than the threshold is cut into
+    chunks that run as separate work, and their partial results are merged).
+    Reading taken: a span of at most ``chunk_blocks`` blocks stays whole; a
+    longer one is cut into k = ceil(n / chunk) equal chunks, each rounded up
+    to a whole KV tile, the last one shorter.  Returns [[lo, hi), ...] in
+    blocks of the span."""
+    if n_blocks <= chunk_blocks:
+        return [[0, n_blocks]]
+    k = _ceil(n_blocks, chunk_blocks)
+    cb = _ceil(_ceil(n_blocks, k), tile_blocks) * tile_blocks
+    return [[s, min(n_blocks, s + cb)] for s in range(0, n_blocks, cb)]
+
+
 def build_plan(parent, node_kv_len, node_page_offsets, node_pages, page_size,
                query_node, query_kv_end, n_q_heads, n_kv_heads, d,
                o: PlannerOptions | None = None):
-    """The whole plan in the canonical form the native planner describes."""
+    """The plan's decisions that the pages define, in canonical form: the
+    edge assignment (Algorithm 1), the groups of the virtual tree with their
+    KV chains, tokens and visible ends, rows and path, the chunks of each
+    group span for the given chunk length, and each token's partial count
+    (one per chunk of every group it belongs to)."""
     o = o or PlannerOptions()
     r = n_q_heads // n_kv_heads
     A = subtree_rows(parent, query_node, r)
     edge, L, rows, bfs = greedy_edges(parent, node_kv_len, A, d, o)
     groups = plan_groups(parent, node_kv_len, query_node, query_kv_end, edge, bfs)
-    bpt = o.kv_tile_tokens // page_size          # blocks per KV tile
+    tile_blocks = o.kv_tile_tokens // page_size
+    chunk = None
+    if o.split_tokens > 0:
+        chunk = _ceil(_ceil(o.split_tokens, page_size), tile_blocks) * tile_blocks
     for g in groups:
         g["blocks"] = group_blocks(g, node_kv_len, node_page_offsets, node_pages,
                                    page_size)
         g["rows"] = len(g["tokens"]) * r
         assert g["rows"] == rows[g["node"]]
         assert g["span"] == L[g["node"]]
+        # path (north-star: tensor cores once a group's stacked query rows
+        # make an MMA tile worth issuing; the threshold is an option)
         if o.force_path == 1:
             g["path"] = "simt"
         elif o.force_path == 2:
             g["path"] = "mma"
         else:
             g["path"] = "mma" if g["rows"] >= o.mma_min_rows else "simt"
-        tile = o.mma_tile_rows if g["path"] == "mma" else o.simt_tile_rows
-        g["qtiles"] = _ceil(g["rows"], tile)
-    # Long-context split: chunk length in blocks, a multiple of one KV tile.
-    work = sum(len(g["blocks"]) * n_kv_heads * g["qtiles"] for g in groups)
-    if o.split_tokens < 0:
-        chunk = max([len(g["blocks"]) for g in groups] + [1])
-        chunk = _ceil(chunk, bpt) * bpt
-    elif o.split_tokens > 0:
-        chunk = _ceil(_ceil(o.split_tokens, page_size), bpt) * bpt
-    else:
-        target = _ceil(work, o.split_waves * o.num_sms)
-        chunk = max(_ceil(o.min_split_tokens, page_size), _ceil(target, bpt) * bpt)
-    chunk = max(chunk, bpt)
-    # Thin tensor-core groups longer than a packable group (more than 8
-    # pages) run packed by kv head: a unit covers four kv heads and one page
-    # of each per tile, so their chunks need no tile alignment.  The
-    # automatic split sizes them for one unit per CTA (two CTAs per SM): the
-    # plan's page-heads over the CTAs, a quarter of that in pages, not below
-    # half the minimum split, in near-equal chunks.
-    def head_thin(g):
-        return (not o.no_pack and g["path"] == "mma" and g["qtiles"] == 1
-                and g["rows"] <= 32 and 32 % r == 0 and n_kv_heads % 4 == 0
-                and len(g["blocks"]) > 8)
-    thin_chunk = max(_ceil(_ceil(o.min_split_tokens, page_size), 2),
-                     _ceil(work, 4 * o.num_sms * 2))
-    for g in groups:
         nb = len(g["blocks"])
-        cg = chunk
-        if o.split_tokens == 0 and head_thin(g):
-            k = _ceil(nb, thin_chunk)
-            g["chunks"] = []
-            s = 0
-            for i in range(k):
-                n_i = nb // k + (1 if i < nb % k else 0)
-                g["chunks"].append([s, s + n_i])
-                s += n_i
-        elif nb <= cg:
-            g["chunks"] = [[0, nb]]
-        else:
-            k = _ceil(nb, cg)
-            cb = _ceil(_ceil(nb, k), bpt) * bpt
-            g["chunks"] = [[s, min(nb, s + cb)] for s in range(0, nb, cb)]
-    # Partial results per query token: one per (group on its path, chunk).
+        g["chunks"] = split_chunks(nb, chunk, tile_blocks) if chunk else [[0, nb]]
     nq = len(query_node)
     count = [0] * nq
     for g in groups:
         for t in g["tokens"]:
             count[t] += len(g["chunks"])
-    # Thin-group packing: up to 4 short single-chunk tensor-core groups of one
-    # kv head share a unit (one page of each per KV tile); at most 32 rows per
-    # slot, and the GQA ratio must divide 32.
-    def packable(g):
-        if o.no_pack or len(g["chunks"]) != 1 or g["qtiles"] != 1:
-            return None
-        nb = len(g["blocks"])
-        if nb < 1 or nb > 8:
-            return None
-        if g["path"] == "mma" and g["rows"] <= 32 and 32 % r == 0:
-            return "mma"
-        return None  # CUDA-core groups are not packed
-    # The longer thin tensor-core groups share units by kv head instead:
-    # four kv heads of the group per unit, one unit per chunk and group of
-    # four kv heads.
-    kinds = [packable(g) for g in groups]
-    n_units = 0
-    for g, k in zip(groups, kinds):
-        if k is not None:
-            continue
-        if head_thin(g):
-            n_units += len(g["chunks"]) * (n_kv_heads // 4)
-        else:
-            n_units += n_kv_heads * g["qtiles"] * len(g["chunks"])
-    # Tensor-core groups of at most half a slot (16 rows, the GQA ratio
-    # dividing 16) pack in two phases, eight to a unit, two per slot, when
-    # the plan then still has at least three units per CTA (two CTAs per
-    # SM); else four to a unit like the others.
-    half = [k == "mma" and g["rows"] <= 16 and 16 % r == 0 for g, k in zip(groups, kinds)]
-    n_full = sum(1 for k, h in zip(kinds, half) if k == "mma" and not h)
-    n_simt = sum(1 for k in kinds if k == "simt")
-    others = n_units + n_kv_heads * (_ceil(n_full, 4) + _ceil(n_simt, 4))
-    with_phases = others + n_kv_heads * _ceil(sum(half), 8)
-    if with_phases >= 3 * o.num_sms * 2:
-        n_units = with_phases
-    else:
-        n_units = n_units + n_kv_heads * (_ceil(n_full + sum(half), 4) + _ceil(n_simt, 4))
     return {
         "edges": edge,
-        "chunk_blocks": chunk,
         "groups": [{k: g[k] for k in ("node", "chain", "span", "tokens", "vis",
-                                      "rows", "path", "qtiles", "chunks")}
+                                      "rows", "path", "chunks")}
                    for g in groups],
         "partials": count,
-        "units": n_units,
         "_blocks": [g["blocks"] for g in groups],
     }
 

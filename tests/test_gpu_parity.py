@@ -16,17 +16,97 @@ pytestmark = pytest.mark.gpu
 
 
 # ----------------------------------------------------------------- the five workloads
-@pytest.mark.parametrize("name,n_sample", [("tiny", 4), ("long", 10), ("wide", 40),
-                                           ("three", 40), ("irreg", 48)])
-def test_workload_parity(name, n_sample):
+@pytest.mark.parametrize("name", ["tiny", "long", "wide", "three"])
+def test_workload_parity_every_token(name):
     spec = W.CONFIGS[name]()
     q, k, v = make_inputs(spec, tail_fill=float("nan"))
     out, lse, stats = run_gpu(spec, q, k, v)
-    toks = sample_tokens(spec, n_sample, seed=7)
-    if name == "irreg":  # every speculative token of a few leaves
-        toks = sorted(set(toks) | set(range(8)) | set(range(spec.n_queries - 8, spec.n_queries)))
+    toks = list(range(spec.n_queries))
     ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
     compare(out, lse, ref, ref_lse, toks)
+
+
+def _stratified_tokens(spec, per_kind=4, n_random=24, seed=7, **options):
+    """Tokens chosen so that every kind of unit the plan holds, masked rows
+    and every partial count are reached; returns (tokens, what was covered)."""
+    import tree_structured_decode_gb300 as ta
+    from schedule_check import check_schedule
+
+    with ta.Plan.from_spec(spec, host_only=1, **options) as p:
+        facts = check_schedule(spec, p.schedule(), collect=True)
+    rng = np.random.default_rng(seed)
+    picks, covered = set(), {}
+    kinds = sorted(set().union(*facts["kinds"]))
+    for kind in kinds:
+        have = [t for t in range(spec.n_queries) if kind in facts["kinds"][t]]
+        chosen = rng.choice(have, size=min(per_kind, len(have)), replace=False).tolist()
+        picks.update(chosen)
+        covered[kind] = chosen
+    masked = np.nonzero(facts["masked"])[0]
+    if len(masked):
+        chosen = rng.choice(masked, size=min(per_kind, len(masked)), replace=False).tolist()
+        picks.update(chosen)
+        covered["masked"] = chosen
+    for c in sorted(set(facts["pcount"].tolist())):
+        have = np.nonzero(facts["pcount"] == c)[0]
+        chosen = rng.choice(have, size=min(per_kind, len(have)), replace=False).tolist()
+        picks.update(chosen)
+        covered[f"partials={c}"] = chosen
+    picks.update(sample_tokens(spec, n_random, seed=seed))
+    return sorted(int(t) for t in picks), covered
+
+
+def test_workload_parity_irregular_stratified():
+    # the irregular tree: too many tokens for the oracle to check all of them,
+    # so the sample reaches every kind of unit the plan holds (full and
+    # half-filled 128-row tiles), rows masked inside a tile (the causal tail of
+    # the 4 speculative tokens, node ends) and every partial count
+    spec = W.config_irregular()
+    toks, covered = _stratified_tokens(spec)
+    for kind in ("mma_full", "mma_half", "masked", "partials=1", "partials=2", "partials=3"):
+        assert kind in covered, (kind, sorted(covered))
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, stats = run_gpu(spec, q, k, v)
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
+    compare(out, lse, ref, ref_lse, toks)
+
+
+@pytest.mark.parametrize("options", [{}, {"split_tokens": 128}, {"num_sms": 4}])
+def test_stratified_tokens_reach_every_packing_kind(options):
+    # short and long thin leaves with 1-3 speculative tokens under a long root:
+    # packed units (one or two phases), kv-head packed units and full tiles
+    rng = np.random.default_rng(3)
+    nleaf = 40
+    lens = [900] + [int(x) for x in rng.integers(1, 129, size=nleaf - 8)] + \
+        [int(x) for x in rng.integers(140, 500, size=8)]
+    ntok = [int(rng.integers(1, 4)) for _ in range(nleaf)]
+    qnode = [v for v in range(1, nleaf + 1) for _ in range(ntok[v - 1])]
+    qend = [max(0, lens[v] - j) for v in range(1, nleaf + 1) for j in range(ntok[v - 1])]
+    spec = W._finish("kinds", [-1] + [0] * nleaf, lens, qnode, qend, 32, 8, 128, seed=4)
+    toks, covered = _stratified_tokens(spec, **options)
+    assert "packed" in covered or "packed_phases" in covered
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, _ = run_gpu(spec, q, k, v, **options)
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
+    compare(out, lse, ref, ref_lse, toks)
+
+
+# ----------------------------------------------------------------- value range
+@pytest.mark.parametrize("options", [{"split_tokens": 64}, {"split_tokens": 64, "merge_mode": 1},
+                                     {"split_tokens": 64, "force_path": 1}])
+def test_values_beyond_fp16_range(options):
+    # V scaled by 2^17 (exact in bf16): |V| up to ~6.5e5, past fp16's 65504,
+    # on a split plan where every token merges several partials.  Scaling V
+    # by c scales the result by c, so out / c must match the oracle on V.
+    spec = W.two_level(700, 5, 90, 8, 2, 128, seed=13)
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    c = 2.0 ** 17
+    vs = (v.float() * c).to(torch.bfloat16)
+    assert torch.equal(vs.float()[torch.isfinite(v)], v.float()[torch.isfinite(v)] * c)
+    out, lse, stats = run_gpu(spec, q, k, vs, **options)
+    assert stats["n_merge_tokens"] == spec.n_queries
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
+    compare(out / c, lse, ref, ref_lse)
 
 
 # ----------------------------------------------------------------- random trees

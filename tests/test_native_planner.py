@@ -1,62 +1,97 @@
-"""The native planner (C ABI, host only) against the reference planner.
+"""The native planner (C ABI, host only) against the reference planner and
+against invariants of its schedule.
 
-Every decision must match exactly: the edge assignment (FastTree review page,
-Algorithm 1 and its cost model), the groups of the virtual tree with their KV
-chains, token lists and visible ends (DeFT notes page, "KV-Guided Tree
-Split"), the path and query tiles of each group, the long-span chunks, the
-partial count of every query token and the number of units."""
+Decisions the pages define must match the reference planner exactly: the edge
+assignment (FastTree review page, Algorithm 1 and its cost model), the groups
+of the virtual tree with their KV chains, token lists, visible ends and rows
+(DeFT notes page, "KV-Guided Tree Split"), each group's path, and, for a
+given chunk length, the long-span chunks and every token's partial count.
+
+How the native scheduler then turns groups into work units (query tiles,
+packing of thin groups, the automatic chunk length, the CTA schedule) is a
+performance choice the pages leave open.  It is checked by invariants on the
+device tables the kernels read (``schedule_check``): every query token and q
+head sees exactly its path's keys, each once, and each result lands exactly
+once."""
 import numpy as np
 import pytest
 
 import workloads as W
 from oracle import planner as P
+from schedule_check import check_schedule
 
 ta = pytest.importorskip("tree_structured_decode_gb300")
+
+PAGE_KEYS = ("node", "chain", "span", "tokens", "vis", "rows", "path")
 
 
 def _native(spec, **opt):
     opt.setdefault("num_sms", 152)
     with ta.Plan.from_spec(spec, host_only=1, **opt) as p:
-        return p.describe(), p.stats()
+        return p.describe(), p.stats(), p.schedule()
 
 
 def _reference(spec, **opt):
-    o = P.PlannerOptions(num_sms=opt.get("num_sms", 152))
-    for k in ("gamma", "beta", "ts_c", "mma_min_rows", "split_tokens", "min_split_tokens",
-              "split_waves", "force_path", "no_pack"):
+    o = P.PlannerOptions()
+    for k in ("gamma", "beta", "ts_c", "mma_min_rows", "force_path"):
         if k in opt:
             setattr(o, k, opt[k])
+    if opt.get("split_tokens", 0) > 0:
+        o.split_tokens = opt["split_tokens"]
     if "ts_q_set" in opt:
         o.ts_q_set = tuple(opt["ts_q_set"])
     if "force_edges" in opt:
         o.edges = tuple(int(x) for x in opt["force_edges"])
-    ref = P.build_plan(spec.parent, spec.node_kv_len, spec.node_page_offsets, spec.node_pages,
-                       spec.page_size, spec.query_node, spec.query_kv_end, spec.n_q_heads,
-                       spec.n_kv_heads, spec.head_dim, o)
-    ref.pop("_blocks")
-    return ref
+    return P.build_plan(spec.parent, spec.node_kv_len, spec.node_page_offsets, spec.node_pages,
+                        spec.page_size, spec.query_node, spec.query_kv_end, spec.n_q_heads,
+                        spec.n_kv_heads, spec.head_dim, o)
+
+
+def _check_chunks(got):
+    """Chunks partition each group's block list in order (any chunk length)."""
+    for g in got["groups"]:
+        ch = g["chunks"]
+        assert ch[0][0] == 0
+        for (a, b), (c, _) in zip(ch, ch[1:]):
+            assert a < b == c
+        assert ch[-1][1] >= ch[-1][0]
+    parts = [0] * len(got["partials"])
+    for g in got["groups"]:
+        for t in g["tokens"]:
+            parts[t] += len(g["chunks"])
+    assert parts == got["partials"]
 
 
 def _same(spec, **opt):
-    got, stats = _native(spec, **opt)
+    got, stats, sched = _native(spec, **opt)
     ref = _reference(spec, **opt)
     assert got["edges"] == ref["edges"]
-    assert got["chunk_blocks"] == ref["chunk_blocks"]
     assert len(got["groups"]) == len(ref["groups"])
     for a, b in zip(got["groups"], ref["groups"]):
-        assert a == b
-    assert got["partials"] == ref["partials"]
-    assert got["units"] == ref["units"]
-    assert stats["n_units"] == ref["units"]
+        assert {k: a[k] for k in PAGE_KEYS} == {k: b[k] for k in PAGE_KEYS}
+    # group blocks: the span in order, page by page (the chunks index them)
+    _check_chunks(got)
+    if opt.get("split_tokens", 0) != 0:  # a given chunk length (or none)
+        for a, b in zip(got["groups"], ref["groups"]):
+            assert a["chunks"] == b["chunks"]
+        assert got["partials"] == ref["partials"]
     assert stats["n_groups"] == len(ref["groups"])
-    return got, stats
+    assert stats["n_units"] == len(sched["units"]) // 8
+    check_schedule(spec, sched, num_sms=opt["num_sms"] if "num_sms" in opt else 152)
+    return got, stats, sched
 
 
 @pytest.mark.parametrize("name", ["tiny", "long", "wide", "three", "irreg"])
 def test_configs_match_reference(name):
     spec = W.CONFIGS[name]()
-    got, stats = _same(spec)
+    got, stats, _ = _same(spec)
     assert stats["unique_kv_tokens"] == int(spec.node_kv_len.sum())
+
+
+@pytest.mark.parametrize("name", ["long", "wide", "three"])
+@pytest.mark.parametrize("split", [-1, 64, 400])
+def test_configs_with_a_given_chunk_length(name, split):
+    _same(W.CONFIGS[name](), split_tokens=split)
 
 
 @pytest.mark.parametrize("seed", range(300))
@@ -79,6 +114,8 @@ def test_random_trees_match_reference(seed):
         opt["beta"] = 3
     if seed % 13 == 5:
         opt["force_path"] = int(rng.integers(1, 3))
+    if seed % 17 == 6:
+        opt["num_sms"] = int(rng.choice([1, 3, 8]))
     _same(spec, **opt)
 
 
@@ -95,24 +132,23 @@ def test_forced_edge_assignments_match_reference(seed):
 @pytest.mark.parametrize("name", ["wide"])
 def test_packing_can_be_disabled(name):
     spec = W.CONFIGS[name]()
-    packed, _ = _same(spec)
-    plain, _ = _same(spec, no_pack=1)
-    assert packed["units"] < plain["units"]
+    packed, ps, _ = _same(spec)
+    plain, qs, _ = _same(spec, no_pack=1)
+    assert ps["n_units"] < qs["n_units"]
     assert packed["groups"] == plain["groups"]
 
 
 def test_planning_is_fast_on_the_irregular_tree():
     spec = W.config_irregular()
-    _, stats = _native(spec)
+    _, stats, _ = _native(spec)
     assert stats["plan_ms"] < 200.0
 
 
 @pytest.mark.parametrize("hq,hkv,ntok", [(16, 4, 1), (8, 4, 2), (32, 8, 6), (64, 4, 3), (16, 2, 2),
                                          (64, 8, 1)])
-def test_kv_head_packing_matches_reference(hq, hkv, ntok):
+def test_kv_head_packing_schedule(hq, hkv, ntok):
     # long thin leaves: groups of <= 32 rows per kv head pack four kv heads to
-    # a unit with a quarter of the automatic chunk (hkv a multiple of 4);
-    # others stay one unit per kv head
+    # a unit (hkv a multiple of 4); others stay one unit per kv head
     rng = np.random.default_rng(hq * 31 + ntok)
     lens = [600] + [int(x) for x in rng.integers(140, 900, size=6)]
     qnode = [v for v in range(1, 7) for _ in range(ntok)]
@@ -131,10 +167,9 @@ def test_draft_token_trees_match_reference(depth, branching, hq, hkv):
 
 @pytest.mark.parametrize("num_sms", [1, 2, 5, 152])
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (32, 4), (64, 4)])
-def test_two_phase_packing_matches_reference(hq, hkv, num_sms):
+def test_two_phase_packing_schedule(hq, hkv, num_sms):
     # short leaves with 1-3 query tokens: groups of at most 16 rows per kv
-    # head pack eight to a unit in two phases while the plan keeps three
-    # units per CTA (few SMs), else four to a unit like the longer ones
+    # head may pack eight to a unit in two phases, else four to a unit
     rng = np.random.default_rng(hq * 7 + num_sms)
     nleaf = 40
     lens = [300] + [int(x) for x in rng.integers(1, 129, size=nleaf)]
@@ -144,3 +179,31 @@ def test_two_phase_packing_matches_reference(hq, hkv, num_sms):
     spec = W._finish("phases", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=hq)
     _same(spec, num_sms=num_sms)
     _same(spec, num_sms=num_sms, no_pack=1)
+
+
+def test_schedule_check_catches_a_planted_fault():
+    # the checker itself: a schedule with one block's valid count lowered, a
+    # row record pointing at another token, or a unit dropped must fail
+    spec = W.random_tree(7, n_nodes=15, max_len=120, hq=8, hkv=2, d=128, max_queries_per_node=3)
+    _, _, sched = _native(spec)
+    check_schedule(spec, sched)
+    faults = []
+    s1 = dict(sched)
+    b = list(s1["blocks"])
+    i = next(k for k in range(1, len(b), 2) if b[k] & 31 > 1)
+    b[i] -= 1
+    s1["blocks"] = b
+    faults.append(s1)
+    s2 = dict(sched)
+    rows = list(s2["rows"])
+    j = next(k for k in range(0, len(rows), 4) if rows[k] >= 0 and rows[k + 3] & 0xFFFFFF == 1)
+    rows[j + 1] -= 1  # visible end one short
+    s2["rows"] = rows
+    faults.append(s2)
+    s3 = dict(sched)
+    s3["units"] = list(sched["units"])[8:]
+    s3["cta_off"] = [max(0, x - 1) for x in sched["cta_off"]]
+    faults.append(s3)
+    for f in faults:
+        with pytest.raises(AssertionError):
+            check_schedule(spec, f)

@@ -153,6 +153,47 @@ def test_coverage_of_greedy_plan_on_configs(name):
     _check_coverage(spec, plan)
 
 
+def test_plan_cost_worked_by_hand():
+    # Root 0 (100 tokens) with children 1 (30 tokens, 3 query rows) and 2 (70
+    # tokens, 20 rows); GQA 1, d = 1, gamma = 64, TS_q in {16, 64, 128},
+    # TS_c = 64.  A = [23, 3, 20].  Per virtual node: Pad(TS_q, rows) * len +
+    # rows * Pad(TS_c, min(len, TS_c)), plus gamma * A[l] for every 0-edge:
+    #  (0, 0): 41*100 + 13*30 + 3*34 + 44*70 + 64*3 + 64*20    = 9144
+    #  (1, 0): 44*100 + 13*130 + 44*70 + 64*20                  = 10450
+    #  (0, 1): 13*100 + 13*30 + 3*34 + 44*170 + 64*3            = 9464
+    #  (1, 1): 0 + 13*130 + 44*170                              = 9170
+    parent, lens = [-1, 0, 0], [100, 30, 70]
+    qnode = [1] * 3 + [2] * 20
+    o = P.PlannerOptions()
+    A = P.subtree_rows(parent, qnode, 1)
+    assert A == [23, 3, 20]
+    want = {(0, 0): 9144, (1, 0): 10450, (0, 1): 9464, (1, 1): 9170}
+    for (e1, e2), c in want.items():
+        assert P.plan_cost(parent, lens, A, 1, [0, e1, e2], o) == c
+        assert P.plan_cost(parent, lens, A, 128, [0, e1, e2], o) == 128 * c
+    # Algorithm 1 on the same tree, by hand: child 1: C0 = 4100 + 390 + 102 +
+    # 192 = 4784 < C1 = 4400 + 1690 = 6090; child 2: C0 = 4100 + 3080 + 1280 =
+    # 8460 < C1 = 1300 + 7480 = 8780: both edges 0, the cheapest plan here.
+    assert P.split_kv_cost(23, 3, 30, 100, 1, o) == 4784
+    assert P.split_q_cost(23, 3, 30, 100, 1, o) == 6090
+    assert P.split_kv_cost(23, 20, 70, 100, 1, o) == 8460
+    assert P.split_q_cost(23, 20, 70, 100, 1, o) == 8780
+    edge, _, rows, _ = P.greedy_edges(parent, lens, A, 1, o)
+    assert edge == [0, 0, 0] and rows == [23, 3, 20]
+
+
+def test_split_chunks_by_hand():
+    # a span of at most one chunk stays whole; a longer one is cut into
+    # ceil(n / chunk) chunks of equal, tile-rounded length, the last shorter
+    assert P.split_chunks(7, 8, 4) == [[0, 7]]
+    assert P.split_chunks(8, 8, 4) == [[0, 8]]
+    assert P.split_chunks(9, 8, 4) == [[0, 8], [8, 9]]       # k = 2, ceil(9/2) = 5 -> 8
+    assert P.split_chunks(250, 28, 4) == [[0, 28], [28, 56], [56, 84], [84, 112], [112, 140],
+                                          [140, 168], [168, 196], [196, 224], [224, 250]]
+    assert P.split_chunks(17, 4, 4) == [[0, 4], [4, 8], [8, 12], [12, 16], [16, 17]]
+    assert P.split_chunks(0, 4, 4) == [[0, 0]]
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_greedy_against_brute_force_proxy(seed):
     spec = W.random_tree(200 + seed, n_nodes=4 + seed, max_len=300, hq=8, hkv=2,

@@ -20,6 +20,7 @@ EXPORTS = (
     "tree_attn_plan_describe", "tree_attn_plan_get_stats", "tree_attn_plan_destroy",
     "tree_attn_status_string", "tree_attn_last_error", "tree_attn_profile_enable",
     "tree_attn_profile_read", "tree_attn_run_static", "tree_attn_append_kv",
+    "tree_attn_plan_describe_schedule",
 )
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -107,6 +108,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.tree_attn_plan_describe.argtypes = [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_size_t,
                                             ctypes.POINTER(ctypes.c_size_t)]
     lib.tree_attn_plan_describe.restype = ctypes.c_int
+    lib.tree_attn_plan_describe_schedule.argtypes = [ctypes.c_void_p, ctypes.c_char_p,
+                                                     ctypes.c_size_t,
+                                                     ctypes.POINTER(ctypes.c_size_t)]
+    lib.tree_attn_plan_describe_schedule.restype = ctypes.c_int
     lib.tree_attn_plan_get_stats.argtypes = [ctypes.c_void_p, ctypes.POINTER(PlanStats)]
     lib.tree_attn_plan_get_stats.restype = ctypes.c_int
     lib.tree_attn_plan_destroy.argtypes = [ctypes.c_void_p]

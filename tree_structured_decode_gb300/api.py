@@ -191,6 +191,17 @@ class Plan:
               "tree_attn_plan_describe")
         return json.loads(buf.value.decode())
 
+    def schedule(self) -> dict:
+        """``tree_attn_plan_describe_schedule``: the device tables of a run
+        (units in schedule order, CTA ranges, blocks, row records, merge
+        items), as flat int lists."""
+        need = ctypes.c_size_t(0)
+        self._lib.tree_attn_plan_describe_schedule(self._handle, None, 0, ctypes.byref(need))
+        buf = ctypes.create_string_buffer(need.value)
+        check(self._lib.tree_attn_plan_describe_schedule(self._handle, buf, need.value, None),
+              "tree_attn_plan_describe_schedule")
+        return json.loads(buf.value.decode())
+
     def stats(self) -> dict:
         s = PlanStats()
         check(self._lib.tree_attn_plan_get_stats(self._handle, ctypes.byref(s)),

@@ -1,8 +1,8 @@
 // Log-sum-exp merge kernel (sm_103a).
 //
-// merge pass: per (query token, q head), fold its partials (O in fp16,
-// lse in fp32):
-//   m = max lse_i, w_i = 2^(lse_i - m), O = sum w_i O_i / sum w_i,
+// merge pass: per (query token, q head), fold its partials (O_i stored in
+// fp16 as O_i / s_i, with lse_i and s_i in fp32):
+//   m = max lse_i, w_i = 2^(lse_i - m), O = sum w_i s_i (O_i / s_i) / sum w_i,
 //   lse = m + log2 sum w_i   (partials keep lse in base 2).
 #include <cuda_runtime.h>
 
@@ -40,22 +40,25 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
     if (idx >= total) continue;
     const MergeItem it = p.items[idx / p.hq];
     const int h = idx % p.hq;
-    const float* lse_h = p.part_lse + (size_t)it.poff * p.hq + h;  // partial k at lse_h[k * hq]
+    const float2* ml_h = p.part_ml + (size_t)it.poff * p.hq + h;  // partial k at ml_h[k * hq]
     const uint16_t* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + l16 * EPL;  // fp16
     float M = -INFINITY, den = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
     for (int k0 = 0; k0 < it.count; k0 += G) {
-      float w[G];
+      float w[G], osc[G];
       uint32_t v[G][NW];
 #pragma unroll
       for (int q = 0; q < G; ++q) {
         const int k = k0 + q;
         w[q] = -INFINITY;
+        osc[q] = 1.f;
 #pragma unroll
         for (int e = 0; e < NW; ++e) v[q][e] = 0u;
         if (k < it.count) {
-          w[q] = __ldcg(lse_h + (size_t)k * p.hq);
+          const float2 ml = __ldcg(ml_h + (size_t)k * p.hq);
+          w[q] = ml.x;
+          osc[q] = ml.y;
           const uint16_t* src = o_h + (size_t)k * p.hq * D;
           if constexpr (NW == 4) {
             const uint4 t = __ldcg(reinterpret_cast<const uint4*>(src));
@@ -79,11 +82,12 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
       for (int q = 0; q < G; ++q) {
         const float wq = exp2f(w[q] - m_new);  // 0 for absent or empty partials
         den += wq;
+        const float wo = wq * osc[q];
 #pragma unroll
         for (int e = 0; e < NW; ++e) {
           const float2 f = ptx::unpack_f16(v[q][e]);
-          acc[2 * e] = fmaf(wq, f.x, acc[2 * e]);
-          acc[2 * e + 1] = fmaf(wq, f.y, acc[2 * e + 1]);
+          acc[2 * e] = fmaf(wo, f.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(wo, f.y, acc[2 * e + 1]);
         }
       }
       M = m_new;

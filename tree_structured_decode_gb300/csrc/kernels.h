@@ -27,6 +27,11 @@ struct MergeItem {
   int32_t tok, poff, count, pad;
 };
 
+// A partial O row whose largest |value| reaches this is stored divided by a
+// power of two s (kept beside its lse), so that fp16 never overflows: the
+// inputs may hold any bf16 value.
+constexpr float kPartialRescaleAt = 32768.f;
+
 // CTAs whose unit ranges travel in the launch parameters (read from the
 // constant bank at start-up instead of a dependent global load).
 constexpr int kInlineCtas = 320;
@@ -41,8 +46,9 @@ struct AttnParams {
   const uint16_t* v;
   float* out;                // [nq][hq][d]
   float* lse;                // [nq][hq] natural log, or null
-  uint16_t* part_o;          // [n_partials][hq][d] fp16 bits (normalised partial O)
-  float* part_lse;           // [n_partials][hq], log2 units
+  uint16_t* part_o;          // [n_partials][hq][d] fp16 bits: normalised partial O / s
+  float2* part_ml;           // [n_partials][hq]: {lse in log2 units, s}; s = 1, or the
+                             // power of two that keeps |O| / s inside the fp16 range
   int32_t* err;              // device error word
   int32_t hq, hkv, gqa, n_units;
   float scale_log2;          // softmax scale * log2(e)
@@ -63,8 +69,8 @@ struct MergeParams {
   const MergeItem* items;
   int32_t n_items, hq;
   int32_t max_count;         // most partials of any merged token
-  const uint16_t* part_o;    // fp16 bits
-  const float* part_lse;
+  const uint16_t* part_o;    // fp16 bits (O / s)
+  const float2* part_ml;     // {lse (log2 units), s}
   float* out;
   float* lse;
 };

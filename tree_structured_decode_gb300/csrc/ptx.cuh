@@ -302,6 +302,15 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t v) {
   return make_float2(lo, hi);
 }
 
+// The divisor s of a partial O row whose largest |value| is amax: 1 below
+// `at`, else the power of two 2^(e - 14) for amax in [2^e, 2^(e+1)), which
+// brings the row into [2^14, 2^15) (inside fp16's range).
+__device__ __forceinline__ float partial_scale(float amax, float at) {
+  if (!(amax >= at)) return 1.f;
+  const int e = (__float_as_int(amax) >> 23) - 127;
+  return __int_as_float((127 + e - 14) << 23);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

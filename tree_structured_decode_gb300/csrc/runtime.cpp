@@ -6,6 +6,7 @@
 #include <chrono>
 #include <cmath>
 #include <cstdlib>
+#include <cstdio>
 #include <cstring>
 #include <new>
 #include <string>
@@ -54,81 +55,74 @@ ta::Options to_options(const tree_attn_options* o) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Lay out every table of the plan in one device buffer and upload it.
+// Partial-result workspace sizes: O (fp16), {lse, scale} and the fused
+// merge's arrival counters.
+struct WorkSizes {
+  size_t o_bytes, ml_bytes, cnt_bytes;
+  size_t total() const { return o_bytes + ml_bytes + cnt_bytes; }
+};
+WorkSizes work_sizes(const ta::HostPlan& h) {
+  const size_t np = (size_t)h.n_partials * h.hq;
+  WorkSizes w;
+  w.o_bytes = align_up(np * h.d * sizeof(uint16_t), 256);
+  w.ml_bytes = align_up(np * sizeof(float2), 256);
+  w.cnt_bytes = h.n_partials ? align_up((size_t)h.nq * h.hq * sizeof(int32_t), 256) : 0;
+  return w;
+}
+
+// Upload the plan's table image and allocate its partial-result workspace.
 tree_attn_status upload(tree_attn_plan_s* P) {
-  const ta::HostPlan& h = P->hp;
-  std::vector<ta::GroupTok> gt(h.gtok.size());
-  for (size_t i = 0; i < gt.size(); ++i)
-    gt[i] = {h.gtok[i], h.gvis[i], h.gpbase[i],
-             ta::pack_pc_slot(h.gtok[i] >= 0 ? h.pcount[h.gtok[i]] : 0, h.gslot[i])};
-  std::vector<int2> blocks(h.blk_page.size());
-  for (size_t i = 0; i < blocks.size(); ++i) blocks[i] = make_int2(h.blk_page[i], h.blk_meta[i]);
-  std::vector<ta::MergeItem> merge(h.merge_tok.size());
-  for (size_t i = 0; i < merge.size(); ++i) {
-    int t = h.merge_tok[i];
-    merge[i] = {t, h.poff[t], h.pcount[t], 0};
-  }
-  struct Sec {
-    const void* src;
-    size_t bytes;
-    size_t off;
-  };
-  Sec secs[8] = {
-      {h.units.data(), h.units.size() * sizeof(ta::UnitDesc), 0},
-      {blocks.data(), blocks.size() * sizeof(int2), 0},
-      {gt.data(), gt.size() * sizeof(ta::GroupTok), 0},
-      {h.cta_off.data(), h.cta_off.size() * sizeof(int32_t), 0},
-      {merge.data(), merge.size() * sizeof(ta::MergeItem), 0},
-      {nullptr, 16 * sizeof(int32_t), 0},  // error word(s)
-      {h.poff.data(), h.poff.size() * sizeof(int32_t), 0},
-      {h.append_dst.data(), h.append_dst.size() * sizeof(int32_t), 0},
-  };
-  size_t off = 0;
-  for (auto& s : secs) {
-    s.off = off;
-    off = align_up(off + std::max<size_t>(s.bytes, 16), 256);
-  }
-  std::vector<uint8_t> host(off, 0);
-  for (auto& s : secs)
-    if (s.src && s.bytes) std::memcpy(host.data() + s.off, s.src, s.bytes);
+  const ta::TableImage& img = P->img;
+  const size_t off = img.bytes.size();
   cudaError_t e = cudaMalloc(&P->dmeta, off);
   if (e != cudaSuccess) {
     P->dmeta = nullptr;
     return set_err(TA_ERR_OOM, std::string("cudaMalloc(plan tables): ") + cudaGetErrorString(e));
   }
   P->meta_bytes = off;
-  e = cudaMemcpy(P->dmeta, host.data(), off, cudaMemcpyHostToDevice);
+  e = cudaMemcpy(P->dmeta, img.bytes.data(), off, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_err(e, "cudaMemcpy(plan tables)");
   uint8_t* b = static_cast<uint8_t*>(P->dmeta);
-  P->d_units = reinterpret_cast<const ta::UnitDesc*>(b + secs[0].off);
-  P->d_blocks = reinterpret_cast<const int2*>(b + secs[1].off);
-  P->d_gtoks = reinterpret_cast<const ta::GroupTok*>(b + secs[2].off);
-  P->d_cta_off = reinterpret_cast<const int32_t*>(b + secs[3].off);
-  P->d_merge = reinterpret_cast<const ta::MergeItem*>(b + secs[4].off);
-  P->d_err = reinterpret_cast<int32_t*>(b + secs[5].off);
-  P->d_tok_poff = reinterpret_cast<const int32_t*>(b + secs[6].off);
-  P->d_append = reinterpret_cast<const int32_t*>(b + secs[7].off);
+  P->d_units = reinterpret_cast<const ta::UnitDesc*>(b + img.off_units);
+  P->d_blocks = reinterpret_cast<const int2*>(b + img.off_blocks);
+  P->d_gtoks = reinterpret_cast<const ta::GroupTok*>(b + img.off_gtoks);
+  P->d_cta_off = reinterpret_cast<const int32_t*>(b + img.off_cta);
+  P->d_merge = reinterpret_cast<const ta::MergeItem*>(b + img.off_merge);
+  P->d_err = reinterpret_cast<int32_t*>(b + img.off_err);
+  P->d_tok_poff = reinterpret_cast<const int32_t*>(b + img.off_poff);
+  P->d_append = reinterpret_cast<const int32_t*>(b + img.off_append);
 
-  const size_t np = (size_t)h.n_partials * h.hq;
-  const size_t o_bytes = align_up(np * h.d * sizeof(uint16_t), 256);  // fp16 partial O
-  const size_t l_bytes = align_up(np * sizeof(float), 256);
-  const size_t c_bytes = h.n_partials ? align_up((size_t)h.nq * h.hq * sizeof(int32_t), 256) : 0;
-  P->work_bytes = o_bytes + l_bytes + c_bytes;
+  const WorkSizes w = work_sizes(P->hp);
+  P->work_bytes = w.total();
   if (P->work_bytes) {
     e = cudaMalloc(&P->dwork, P->work_bytes);
     if (e != cudaSuccess) {
       P->dwork = nullptr;
       return set_err(TA_ERR_OOM, std::string("cudaMalloc(workspace): ") + cudaGetErrorString(e));
     }
-    P->d_part_o = static_cast<uint16_t*>(P->dwork);
-    P->d_part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(P->dwork) + o_bytes);
-    if (c_bytes) {
-      P->d_merge_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(P->dwork) + o_bytes + l_bytes);
-      P->merge_cnt_bytes = c_bytes;
-      e = cudaMemset(P->d_merge_cnt, 0, c_bytes);
+    uint8_t* wb = static_cast<uint8_t*>(P->dwork);
+    P->d_part_o = reinterpret_cast<uint16_t*>(wb);
+    P->d_part_ml = reinterpret_cast<float2*>(wb + w.o_bytes);
+    if (w.cnt_bytes) {
+      P->d_merge_cnt = reinterpret_cast<int32_t*>(wb + w.o_bytes + w.ml_bytes);
+      P->merge_cnt_bytes = w.cnt_bytes;
+      e = cudaMemset(P->d_merge_cnt, 0, w.cnt_bytes);
       if (e != cudaSuccess) return cuda_err(e, "cudaMemset(merge counters)");
     }
   }
+  return TA_OK;
+}
+
+// The plan's device memory and tables belong to the device that was current
+// when it was made; launching it from another device would read them there.
+tree_attn_status check_device(const tree_attn_plan_s* P) {
+  int cur = -1;
+  const cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
+  if (cur != P->device)
+    return set_err(TA_ERR_INVALID_ARG, "the current device (" + std::to_string(cur) +
+                                           ") is not the plan's device (" +
+                                           std::to_string(P->device) + ")");
   return TA_OK;
 }
 
@@ -151,6 +145,51 @@ void release(tree_attn_plan_s* P) {
 
 namespace ta {
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+TableImage build_table_image(const HostPlan& h) {
+  TableImage img;
+  std::vector<GroupTok> gt(h.gtok.size());
+  for (size_t i = 0; i < gt.size(); ++i)
+    gt[i] = {h.gtok[i], h.gvis[i], h.gpbase[i],
+             pack_pc_slot(h.gtok[i] >= 0 ? h.pcount[h.gtok[i]] : 0, h.gslot[i])};
+  std::vector<int2> blocks(h.blk_page.size());
+  for (size_t i = 0; i < blocks.size(); ++i) blocks[i] = make_int2(h.blk_page[i], h.blk_meta[i]);
+  std::vector<MergeItem> merge(h.merge_tok.size());
+  for (size_t i = 0; i < merge.size(); ++i) {
+    const int t = h.merge_tok[i];
+    merge[i] = {t, h.poff[t], h.pcount[t], 0};
+  }
+  struct Sec {
+    const void* src;
+    size_t bytes;
+    size_t* off;
+  } secs[8] = {
+      {h.units.data(), h.units.size() * sizeof(UnitDesc), &img.off_units},
+      {blocks.data(), blocks.size() * sizeof(int2), &img.off_blocks},
+      {gt.data(), gt.size() * sizeof(GroupTok), &img.off_gtoks},
+      {h.cta_off.data(), h.cta_off.size() * sizeof(int32_t), &img.off_cta},
+      {merge.data(), merge.size() * sizeof(MergeItem), &img.off_merge},
+      {nullptr, 16 * sizeof(int32_t), &img.off_err},  // error word(s), zero
+      {h.poff.data(), h.poff.size() * sizeof(int32_t), &img.off_poff},
+      {h.append_dst.data(), h.append_dst.size() * sizeof(int32_t), &img.off_append},
+  };
+  size_t off = 0;
+  for (auto& sec : secs) {
+    *sec.off = off;
+    off = align_up(off + std::max<size_t>(sec.bytes, 16), 256);
+  }
+  img.bytes.assign(off, 0);
+  for (auto& sec : secs)
+    if (sec.src && sec.bytes) std::memcpy(img.bytes.data() + *sec.off, sec.src, sec.bytes);
+  img.n_units = h.units.size();
+  img.n_blocks = blocks.size();
+  img.n_gtoks = gt.size();
+  img.n_cta = h.cta_off.size();
+  img.n_merge = merge.size();
+  img.n_tok = (size_t)h.nq;
+  img.max_count = h.pcount.empty() ? 0 : *std::max_element(h.pcount.begin(), h.pcount.end());
+  return img;
+}
 }  // namespace ta
 
 extern "C" {
@@ -217,6 +256,12 @@ tree_attn_status tree_attn_plan(const int32_t* parent, int32_t n_nodes, const in
   }
   P->host_only = host_only;
   P->device = device;
+  try {
+    P->img = ta::build_table_image(P->hp);
+  } catch (const std::bad_alloc&) {
+    delete P;
+    return set_err(TA_ERR_OOM, "host allocation failed while building the plan tables");
+  }
   if (!host_only) {
     st = upload(P);
     if (st != TA_OK) {
@@ -242,6 +287,10 @@ tree_attn_status tree_attn_append_kv(tree_attn_plan_t P, const void* k_new, cons
   auto mis = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
   if (mis(k_new) || mis(v_new) || mis(k_pages) || mis(v_pages))
     return set_err(TA_ERR_ALIGNMENT, "k_new, v_new, k_pages and v_pages must be 16-byte aligned");
+  {
+    const tree_attn_status ds = check_device(P);
+    if (ds != TA_OK) return ds;
+  }
   cudaError_t e = ta::launch_append_kv(static_cast<const uint16_t*>(k_new),
                                        static_cast<const uint16_t*>(v_new), P->d_append, h.nq,
                                        h.hkv, h.d, static_cast<uint16_t*>(k_pages),
@@ -263,6 +312,10 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
   auto mis = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
   if (mis(q, 16) || mis(k_pages, 16) || mis(v_pages, 16) || mis(out, 16) || mis(lse, 4))
     return set_err(TA_ERR_ALIGNMENT, "q/k_pages/v_pages/out must be 16-byte aligned, lse 4-byte");
+  {
+    const tree_attn_status ds = check_device(P);
+    if (ds != TA_OK) return ds;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ta::AttnParams ap{};
   ap.units = P->d_units;
@@ -275,7 +328,7 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
   ap.out = out;
   ap.lse = lse;
   ap.part_o = P->d_part_o;
-  ap.part_lse = P->d_part_lse;
+  ap.part_ml = P->d_part_ml;
   ap.err = P->d_err;
   ap.hq = h.hq;
   ap.hkv = h.hkv;
@@ -306,9 +359,9 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
     mp.items = P->d_merge;
     mp.n_items = (int32_t)h.merge_tok.size();
     mp.hq = h.hq;
-    mp.max_count = h.pcount.empty() ? 0 : *std::max_element(h.pcount.begin(), h.pcount.end());
+    mp.max_count = P->img.max_count;
     mp.part_o = P->d_part_o;
-    mp.part_lse = P->d_part_lse;
+    mp.part_ml = P->d_part_ml;
     mp.out = out;
     mp.lse = lse;
     e = ta::launch_lse_merge(mp, h.d, s);
@@ -392,6 +445,44 @@ tree_attn_status tree_attn_plan_describe(tree_attn_plan_t P, char* buf, size_t c
   g_last_error.clear();
   if (!P) return set_err(TA_ERR_INVALID_ARG, "plan is NULL");
   std::string s = ta::describe_json(P->hp);
+  if (needed) *needed = s.size() + 1;
+  if (!buf || cap < s.size() + 1) return set_err(TA_ERR_BUFFER_TOO_SMALL, "describe buffer too small");
+  std::memcpy(buf, s.c_str(), s.size() + 1);
+  return TA_OK;
+}
+
+tree_attn_status tree_attn_plan_describe_schedule(tree_attn_plan_t P, char* buf, size_t cap,
+                                                  size_t* needed) {
+  g_last_error.clear();
+  if (!P) return set_err(TA_ERR_INVALID_ARG, "plan is NULL");
+  const ta::TableImage& img = P->img;
+  const ta::HostPlan& h = P->hp;
+  std::string s;
+  s.reserve(64 + img.bytes.size() * 3);
+  auto ints = [&](const char* key, size_t off, size_t n_ints) {
+    s += ",\"";
+    s += key;
+    s += "\":[";
+    char b[16];
+    for (size_t i = 0; i < n_ints; ++i) {
+      int32_t v;
+      std::memcpy(&v, img.bytes.data() + off + 4 * i, 4);
+      std::snprintf(b, sizeof b, i ? ",%d" : "%d", v);
+      s += b;
+    }
+    s += ']';
+  };
+  s += "{\"hq\":" + std::to_string(h.hq) + ",\"hkv\":" + std::to_string(h.hkv) +
+       ",\"gqa\":" + std::to_string(h.gqa) + ",\"d\":" + std::to_string(h.d) +
+       ",\"grid\":" + std::to_string(h.grid) + ",\"n_partials\":" + std::to_string(h.n_partials) +
+       ",\"num_pages\":" + std::to_string(h.num_pages) + ",\"n_tokens\":" + std::to_string(h.nq);
+  ints("units", img.off_units, img.n_units * sizeof(ta::UnitDesc) / 4);
+  ints("cta_off", img.off_cta, img.n_cta);
+  ints("blocks", img.off_blocks, img.n_blocks * 2);
+  ints("rows", img.off_gtoks, img.n_gtoks * sizeof(ta::GroupTok) / 4);
+  ints("merge", img.off_merge, img.n_merge * sizeof(ta::MergeItem) / 4);
+  ints("poff", img.off_poff, img.n_tok);
+  s += '}';
   if (needed) *needed = s.size() + 1;
   if (!buf || cap < s.size() + 1) return set_err(TA_ERR_BUFFER_TOO_SMALL, "describe buffer too small");
   std::memcpy(buf, s.c_str(), s.size() + 1);

@@ -6,13 +6,13 @@
 // memory budget at start-up.  For them this entry point uses one fixed
 // scratch array compiled into the library (TREE_ATTN_STATIC_SCRATCH_BYTES),
 // and works even with a plan made with host_only = 1, which holds no device
-// memory.  Every call copies the plan's tables into the scratch, packs them
-// with a small kernel (which also clears the error word), and runs the same
-// partial-attention and merge kernels as tree_attn_run() with their tables
-// and partial results in the scratch.
+// memory.  Every call copies the plan's table image (built once, when the
+// plan was made) into the scratch with one copy, clears the fused merge's
+// arrival counters, and runs the same partial-attention and merge kernels as
+// tree_attn_run() with their tables and partial results in the scratch.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <algorithm>
 #include <cstdint>
 #include <mutex>
 #include <string>
@@ -30,45 +30,50 @@ constexpr size_t kScratchBytes = TREE_ATTN_STATIC_SCRATCH_BYTES;
 // (on the host it names a stand-in); scratch_base() resolves the address.
 static __device__ __align__(256) unsigned char g_static_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+// The scratch address is looked up once per device and context: a context
+// made anew (after cudaDeviceReset, say) loads the module again, and the
+// address is looked up again.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
 
-// Device address of the scratch on `dev` (the current device), looked up once
-// per device.
+constexpr int kMaxDevices = 64;
+struct ScratchAddr {
+  CUcontext ctx;
+  void* addr;
+};
+std::mutex g_scratch_mu;
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch on `dev` (the current device).
 cudaError_t scratch_base(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CtxGetCurrentFn get = ctx_get_current();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  CUcontext ctx = nullptr;
+  if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (!a.addr || !ctx || a.ctx != ctx) {
     void* ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = ptr;
+    if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    a.addr = ptr;
+    a.ctx = ctx;
   }
-  *out = g_scratch_addr[dev];
+  *out = a.addr;
   return cudaSuccess;
-}
-
-// Interleave the plan's flat tables into the records the kernels read, and
-// clear the error words.
-__global__ void pack_tables(const int32_t* blk_page, const int32_t* blk_meta, int nblk,
-                            int2* blocks, const int32_t* gtok, const int32_t* gvis,
-                            const int32_t* gpbase, const int32_t* gslot, int ntok, GroupTok* gtoks,
-                            const int32_t* merge_tok, const int32_t* poff, const int32_t* pcount,
-                            int nmerge, MergeItem* merge, int32_t* err, int32_t* cnt, int ncnt) {
-  const int n = max(max(nblk, ntok), max(nmerge, ncnt));
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    if (i < nblk) blocks[i] = make_int2(blk_page[i], blk_meta[i]);
-    if (i < ntok)
-      gtoks[i] = GroupTok{gtok[i], gvis[i], gpbase[i],
-                          pack_pc_slot(gtok[i] >= 0 ? pcount[gtok[i]] : 0, gslot[i])};
-    if (i < ncnt) cnt[i] = 0;  // fused-merge arrival counters start at zero
-    if (i < nmerge) {
-      const int t = merge_tok[i];
-      merge[i] = MergeItem{t, poff[t], pcount[t], 0};
-    }
-  }
-  if (blockIdx.x == 0 && threadIdx.x < 16) err[threadIdx.x] = 0;
 }
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -88,6 +93,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   set_last_error("");
   if (!P) return fail(TA_ERR_INVALID_ARG, "plan is NULL");
   const HostPlan& h = P->hp;
+  const TableImage& img = P->img;
   if (h.nq == 0) return TA_OK;
   if (!q || !out || (h.num_pages > 0 && (!k_pages || !v_pages)))
     return fail(TA_ERR_INVALID_ARG, "q, k_pages, v_pages and out must be non-NULL");
@@ -95,32 +101,17 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   if (mis(q, 16) || mis(k_pages, 16) || mis(v_pages, 16) || mis(out, 16) || mis(lse, 4))
     return fail(TA_ERR_ALIGNMENT, "q/k_pages/v_pages/out must be 16-byte aligned, lse 4-byte");
 
-  // ---- scratch layout (every section 256-byte aligned)
-  const size_t nu = h.units.size(), nblk = h.blk_page.size(), ntok = h.gtok.size();
-  const size_t nmerge = h.merge_tok.size(), nq = (size_t)h.nq;
+  // ---- scratch layout: the table image, then the partial results (every
+  // section 256-byte aligned)
   const size_t np = (size_t)h.n_partials * (size_t)h.hq;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    const size_t o = off;
-    off += up256(bytes ? bytes : 16);
-    return o;
-  };
-  const size_t o_units = take(nu * sizeof(UnitDesc));
-  const size_t o_cta = take(h.cta_off.size() * sizeof(int32_t));
-  const size_t o_bpage = take(nblk * 4), o_bmeta = take(nblk * 4), o_blocks = take(nblk * 8);
-  const size_t o_gtok = take(ntok * 4), o_gvis = take(ntok * 4), o_gpb = take(ntok * 4);
-  const size_t o_gslot = take(ntok * 4);
-  const size_t o_gtoks = take(ntok * sizeof(GroupTok));
-  const size_t o_mtok = take(nmerge * 4), o_poff = take(nq * 4), o_pcnt = take(nq * 4);
-  const size_t o_merge = take(nmerge * sizeof(MergeItem));
-  const size_t o_err = take(16 * sizeof(int32_t));
-  const size_t o_po = take(np * (size_t)h.d * sizeof(uint16_t));  // fp16 partial O
-  const size_t o_pl = take(np * sizeof(float));
-  const size_t ncnt = h.n_partials ? nq * (size_t)h.hq : 0;
-  const size_t o_cnt = take(ncnt * sizeof(int32_t));
-  if (off > kScratchBytes)
+  const size_t o_po = up256(img.bytes.size());
+  const size_t o_pml = o_po + up256(np * (size_t)h.d * sizeof(uint16_t));  // fp16 partial O
+  const size_t o_cnt = o_pml + up256(np * sizeof(float2));
+  const size_t ncnt = h.n_partials ? (size_t)h.nq * (size_t)h.hq : 0;
+  const size_t need = o_cnt + up256(ncnt * sizeof(int32_t));
+  if (need > kScratchBytes)
     return fail(TA_ERR_UNSUPPORTED,
-                "this plan needs " + std::to_string(off) + " bytes of scratch; the static scratch "
+                "this plan needs " + std::to_string(need) + " bytes of scratch; the static scratch "
                 "holds " + std::to_string(kScratchBytes) + " (TREE_ATTN_STATIC_SCRATCH_BYTES); use "
                 "tree_attn_run() with a device plan instead");
 
@@ -135,81 +126,52 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   uint8_t* base = static_cast<uint8_t*>(basev);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // ---- tables: host -> scratch, then pack
-  struct Copy {
-    size_t dst;
-    const void* src;
-    size_t bytes;
-  } copies[] = {
-      {o_units, h.units.data(), nu * sizeof(UnitDesc)},
-      {o_cta, h.cta_off.data(), h.cta_off.size() * sizeof(int32_t)},
-      {o_bpage, h.blk_page.data(), nblk * 4},
-      {o_bmeta, h.blk_meta.data(), nblk * 4},
-      {o_gtok, h.gtok.data(), ntok * 4},
-      {o_gvis, h.gvis.data(), ntok * 4},
-      {o_gpb, h.gpbase.data(), ntok * 4},
-      {o_gslot, h.gslot.data(), ntok * 4},
-      {o_mtok, h.merge_tok.data(), nmerge * 4},
-      {o_poff, h.poff.data(), nq * 4},
-      {o_pcnt, h.pcount.data(), nq * 4},
-  };
-  for (const Copy& c : copies) {
-    if (!c.bytes) continue;
-    e = cudaMemcpyAsync(base + c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
+  // ---- tables: one copy of the image (its error words are zero), then the
+  // fused merge's counters start at zero
+  e = cudaMemcpyAsync(base, img.bytes.data(), img.bytes.size(), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
+  if (ncnt) {
+    e = cudaMemsetAsync(base + o_cnt, 0, ncnt * sizeof(int32_t), s);
+    if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
   }
-  const size_t nmax = std::max(std::max(nblk, ntok), std::max(nmerge, ncnt));
-  const int pack_blocks = (int)std::min<size_t>(std::max<size_t>((nmax + 255) / 256, 1), 1024);
-  pack_tables<<<pack_blocks, 256, 0, s>>>(
-      reinterpret_cast<const int32_t*>(base + o_bpage), reinterpret_cast<const int32_t*>(base + o_bmeta),
-      (int)nblk, reinterpret_cast<int2*>(base + o_blocks),
-      reinterpret_cast<const int32_t*>(base + o_gtok), reinterpret_cast<const int32_t*>(base + o_gvis),
-      reinterpret_cast<const int32_t*>(base + o_gpb), reinterpret_cast<const int32_t*>(base + o_gslot),
-      (int)ntok,
-      reinterpret_cast<GroupTok*>(base + o_gtoks), reinterpret_cast<const int32_t*>(base + o_mtok),
-      reinterpret_cast<const int32_t*>(base + o_poff), reinterpret_cast<const int32_t*>(base + o_pcnt),
-      (int)nmerge, reinterpret_cast<MergeItem*>(base + o_merge),
-      reinterpret_cast<int32_t*>(base + o_err), reinterpret_cast<int32_t*>(base + o_cnt), (int)ncnt);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("table pack launch: ") + cudaGetErrorString(e));
 
   // ---- the same kernels as tree_attn_run(), tables and partials in the scratch
   AttnParams ap{};
-  ap.units = reinterpret_cast<const UnitDesc*>(base + o_units);
-  ap.blocks = reinterpret_cast<const int2*>(base + o_blocks);
-  ap.gtoks = reinterpret_cast<const GroupTok*>(base + o_gtoks);
-  ap.cta_off = reinterpret_cast<const int32_t*>(base + o_cta);
+  ap.units = reinterpret_cast<const UnitDesc*>(base + img.off_units);
+  ap.blocks = reinterpret_cast<const int2*>(base + img.off_blocks);
+  ap.gtoks = reinterpret_cast<const GroupTok*>(base + img.off_gtoks);
+  ap.cta_off = reinterpret_cast<const int32_t*>(base + img.off_cta);
   ap.q = static_cast<const uint16_t*>(q);
   ap.k = static_cast<const uint16_t*>(k_pages);
   ap.v = static_cast<const uint16_t*>(v_pages);
   ap.out = out;
   ap.lse = lse;
   ap.part_o = reinterpret_cast<uint16_t*>(base + o_po);
-  ap.part_lse = reinterpret_cast<float*>(base + o_pl);
-  ap.err = reinterpret_cast<int32_t*>(base + o_err);
+  ap.part_ml = reinterpret_cast<float2*>(base + o_pml);
+  ap.err = reinterpret_cast<int32_t*>(base + img.off_err);
   ap.hq = h.hq;
   ap.hkv = h.hkv;
   ap.gqa = h.gqa;
-  ap.n_units = (int32_t)nu;
+  ap.n_units = (int32_t)img.n_units;
   ap.scale_log2 = h.scale * 1.4426950408889634f;
   ap.wait_timeout_ns = (long long)h.opt.wait_timeout_us * 1000ll;
   ap.debug_stuck_wait = h.opt.debug_stuck_wait;
   ap.merge_cnt = reinterpret_cast<int32_t*>(base + o_cnt);
-  ap.tok_poff = reinterpret_cast<const int32_t*>(base + o_poff);
+  ap.tok_poff = reinterpret_cast<const int32_t*>(base + img.off_poff);
   ap.merge_fused = h.opt.merge_mode == 1 ? 1 : 0;
   ap.cta_inline = h.grid <= ta::kInlineCtas ? 1 : 0;
   if (ap.cta_inline)
     for (int c = 0; c <= h.grid; ++c) ap.cta_off_inline[c] = h.cta_off[c];
   e = launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
   if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("partial attention launch: ") + cudaGetErrorString(e));
-  if (nmerge && !ap.merge_fused) {
+  if (img.n_merge && !ap.merge_fused) {
     MergeParams mp{};
-    mp.items = reinterpret_cast<const MergeItem*>(base + o_merge);
-    mp.n_items = (int32_t)nmerge;
+    mp.items = reinterpret_cast<const MergeItem*>(base + img.off_merge);
+    mp.n_items = (int32_t)img.n_merge;
     mp.hq = h.hq;
-    mp.max_count = h.pcount.empty() ? 0 : *std::max_element(h.pcount.begin(), h.pcount.end());
+    mp.max_count = img.max_count;
     mp.part_o = ap.part_o;
-    mp.part_lse = ap.part_lse;
+    mp.part_ml = ap.part_ml;
     mp.out = out;
     mp.lse = lse;
     e = launch_lse_merge(mp, h.d, s);

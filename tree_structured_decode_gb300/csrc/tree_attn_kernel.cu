@@ -317,9 +317,10 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 }
 
 // ---------------------------------------------------------- fused merge
-// After a row's partial (O normalised, lse in base 2) is written, its writer
-// counts it in; the writer of the row's last partial folds all of them:
-//   m = max lse_i, w_i = 2^(lse_i - m), O = sum w_i O_i / sum w_i,
+// After a row's partial (O normalised and stored as O / s, lse in base 2) is
+// written, its writer counts it in; the writer of the row's last partial
+// folds all of them:
+//   m = max lse_i, w_i = 2^(lse_i - m), O = sum w_i s_i (O_i / s_i) / sum w_i,
 //   lse = m + log2 sum w_i
 // (DeFT notes page, "Tree-Topology-Aware Global Reduction Strategy"), writes
 // the output row and resets the counter for the next run.  Release: a fence
@@ -335,14 +336,14 @@ __device__ __noinline__ void merge_row_thread(const AttnParams& p, const GroupTo
   __threadfence();
   const int poff = __ldcg(p.tok_poff + gt.tok);
   float m = -INFINITY;
-  for (int k = 0; k < gt.pcount(); ++k) m = fmaxf(m, __ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h));
+  for (int k = 0; k < gt.pcount(); ++k) m = fmaxf(m, __ldcg(p.part_ml + (size_t)(poff + k) * p.hq + h).x);
   float* dst = p.out + (size_t)idx * D;
   float den = 0.f;
   if (m == -INFINITY) {
     for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   } else {
     for (int k = 0; k < gt.pcount(); ++k)
-      den += ptx::ex2(__ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h) - m);
+      den += ptx::ex2(__ldcg(p.part_ml + (size_t)(poff + k) * p.hq + h).x - m);
     const float inv = 1.f / den;
 #pragma unroll 1
     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -351,7 +352,8 @@ __device__ __noinline__ void merge_row_thread(const AttnParams& p, const GroupTo
       for (int e = 0; e < 8; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int k = 0; k < gt.pcount(); ++k) {
         const size_t slot = (size_t)(poff + k) * p.hq + h;
-        const float w = ptx::ex2(__ldcg(p.part_lse + slot) - m);
+        const float2 ml = __ldcg(p.part_ml + slot);
+        const float w = ptx::ex2(ml.x - m) * ml.y;
         const uint4* src = reinterpret_cast<const uint4*>(p.part_o + slot * D + c0);  // fp16
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -393,21 +395,23 @@ __device__ __noinline__ void merge_row_warp(const AttnParams& p, const GroupTok&
   __threadfence();
   const int poff = __ldcg(p.tok_poff + gt.tok);
   float m = -INFINITY;
-  for (int k = 0; k < gt.pcount(); ++k) m = fmaxf(m, __ldcg(p.part_lse + (size_t)(poff + k) * p.hq + h));
+  for (int k = 0; k < gt.pcount(); ++k) m = fmaxf(m, __ldcg(p.part_ml + (size_t)(poff + k) * p.hq + h).x);
   float acc[EPL], den = 0.f;
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   if (m != -INFINITY) {
     for (int k = 0; k < gt.pcount(); ++k) {
       const size_t slot = (size_t)(poff + k) * p.hq + h;
-      const float w = ptx::ex2(__ldcg(p.part_lse + slot) - m);
+      const float2 ml = __ldcg(p.part_ml + slot);
+      const float w = ptx::ex2(ml.x - m);
       den += w;
+      const float wo = w * ml.y;
       const uint32_t* src = reinterpret_cast<const uint32_t*>(p.part_o + slot * D + lane * EPL);
 #pragma unroll
       for (int e = 0; e < EPL; e += 2) {
         const float2 v = ptx::unpack_f16(__ldcg(src + e / 2));
-        acc[e] = fmaf(w, v.x, acc[e]);
-        acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+        acc[e] = fmaf(wo, v.x, acc[e]);
+        acc[e + 1] = fmaf(wo, v.y, acc[e + 1]);
       }
     }
   }
@@ -637,9 +641,16 @@ __device__ __noinline__ void simt_unit(const AttnParams& p, const UnitDesc& u, u
       } else {
         const size_t ps = (size_t)(gt.pbase + u.chunk) * p.hq + h;
         uint32_t* dst = reinterpret_cast<uint32_t*>(p.part_o + ps * D + lane * EPL);
-        if (lane == 0) p.part_lse[ps] = lse2;
+        float am = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; e += 2) dst[e / 2] = ptx::pack_f16(O[e] * inv, O[e + 1] * inv);
+        for (int e = 0; e < EPL; ++e) am = fmaxf(am, fabsf(O[e] * inv));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, off));
+        const float s_o = ptx::partial_scale(am, kPartialRescaleAt);
+        const float inv_s = inv / s_o;
+        if (lane == 0) p.part_ml[ps] = make_float2(lse2, s_o);
+#pragma unroll
+        for (int e = 0; e < EPL; e += 2) dst[e / 2] = ptx::pack_f16(O[e] * inv_s, O[e + 1] * inv_s);
       }
       if (gt.pbase >= 0 && p.merge_fused) merge_row_warp<D>(p, gt, h, lane);
     }
@@ -693,12 +704,14 @@ __device__ __forceinline__ void load_q(const QRow& r, uint32_t qb, int tid) {
   ptx::cp_async_commit();
 }
 
-// Write columns [c0, c0 + N) of row `grow`'s result (normalised O, and lse
-// when with_lse) to the output (fp32) or to its partial slot (fp16).
+// Write columns [c0, c0 + N) of row `grow`'s result, normalised O times
+// `inv`, to the output (fp32, and its lse when with_lse) or to its partial
+// slot (fp16).  For a partial row, amax accumulates the largest |O| written,
+// so that the caller can tell when fp16 overflowed.
 template <int D, int N>
 __device__ __forceinline__ void write_row_cols(const AttnParams& p, const UnitDesc& u, int grow,
                                                const GroupTok& gt, const float* o, int c0, float inv,
-                                               float lse2, bool with_lse) {
+                                               float lse2, bool with_lse, float& amax) {
   const int h = unit_head(p, u, grow);
   if (gt.pbase < 0) {
     float* dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
@@ -710,12 +723,38 @@ __device__ __forceinline__ void write_row_cols(const AttnParams& p, const UnitDe
   } else {
     const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
     uint16_t* dst = p.part_o + slot * D;
-    if (with_lse) p.part_lse[slot] = lse2;
+#pragma unroll
+    for (int c = 0; c < N; c += 2) amax = ptx::max3(amax, fabsf(o[c]), fabsf(o[c + 1]));
 #pragma unroll
     for (int c = 0; c < N; c += 8)
       *reinterpret_cast<uint4*>(dst + c0 + c) =
           make_uint4(ptx::pack_f16(o[c] * inv, o[c + 1] * inv), ptx::pack_f16(o[c + 2] * inv, o[c + 3] * inv),
                      ptx::pack_f16(o[c + 4] * inv, o[c + 5] * inv), ptx::pack_f16(o[c + 6] * inv, o[c + 7] * inv));
+  }
+}
+
+// A partial row whose normalised O reached kPartialRescaleAt is written again
+// from TMEM (O is still there) divided by its scale s, which the caller
+// stores beside the lse.  Called by the whole warp (the TMEM loads are
+// warp-wide); only rows with `mine` write.  Rare: kept out of line.
+template <int D>
+__device__ __noinline__ void rewrite_scaled_partial(const AttnParams& p, const UnitDesc& u, int grow,
+                                                    const GroupTok& gt, uint32_t o_tmem, float inv_s,
+                                                    bool mine) {
+#pragma unroll 1
+  for (int c = 0; c < D; c += 32) {
+    float o[32];
+    ptx::tmem_ld32(o_tmem + c, o);
+    ptx::tmem_wait_ld();
+    if (mine) {
+      const int h = unit_head(p, u, grow);
+      uint16_t* dst = p.part_o + ((size_t)(gt.pbase + u.chunk) * p.hq + h) * D;
+#pragma unroll
+      for (int e = 0; e < 32; e += 8)
+        *reinterpret_cast<uint4*>(dst + c + e) = make_uint4(
+            ptx::pack_f16(o[e] * inv_s, o[e + 1] * inv_s), ptx::pack_f16(o[e + 2] * inv_s, o[e + 3] * inv_s),
+            ptx::pack_f16(o[e + 4] * inv_s, o[e + 5] * inv_s), ptx::pack_f16(o[e + 6] * inv_s, o[e + 7] * inv_s));
+    }
   }
 }
 
@@ -761,7 +800,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         } else {
           const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
           uint16_t* dst = p.part_o + slot * D;
-          p.part_lse[slot] = -INFINITY;
+          p.part_ml[slot] = make_float2(-INFINITY, 1.f);
           for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
         }
         if (gt.pbase >= 0 && p.merge_fused) merge_row_thread<D>(p, gt, h);
@@ -988,6 +1027,8 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     if (ok && wact) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const float lse2 = l_run > 0.f ? m_run + __log2f(l_run) : -INFINITY;
+      const bool wr = row_ok && !*sh.abort_flag;
+      float amax = 0.f;
       // O in 64-column halves: one TMEM round trip per half
 #pragma unroll
       for (int c = 0; c < D / 32; c += 2) {
@@ -995,11 +1036,19 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         ptx::tmem_ld32(o_tmem + c * 32, o0);
         ptx::tmem_ld32(o_tmem + c * 32 + 32, o1);
         ptx::tmem_wait_ld();
-        if (row_ok && !*sh.abort_flag) {
-          write_row_cols<D, 32>(p, u, u.row0 + tid, gt_row, o0, c * 32, inv, lse2, c == 0);
-          write_row_cols<D, 32>(p, u, u.row0 + tid, gt_row, o1, c * 32 + 32, inv, lse2, false);
+        if (wr) {
+          write_row_cols<D, 32>(p, u, u.row0 + tid, gt_row, o0, c * 32, inv, lse2, c == 0, amax);
+          write_row_cols<D, 32>(p, u, u.row0 + tid, gt_row, o1, c * 32 + 32, inv, lse2, false, amax);
         }
       }
+      // a partial row out of fp16's range is stored again, divided by s
+      const bool part = wr && gt_row.pbase >= 0;
+      const float s_o = part ? ptx::partial_scale(amax * inv, kPartialRescaleAt) : 1.f;
+      if (__any_sync(0xffffffffu, s_o != 1.f))
+        rewrite_scaled_partial<D>(p, u, u.row0 + tid, gt_row, o_tmem, inv / s_o, s_o != 1.f);
+      if (part)
+        p.part_ml[(size_t)(gt_row.pbase + u.chunk) * p.hq + unit_head(p, u, u.row0 + tid)] =
+            make_float2(lse2, s_o);
     }
     ptx::tc_fence_before();
     ptx::mbar_arrive(B.o_empty());  // O is free before the (rare, slow) merge
@@ -1148,18 +1197,17 @@ cudaError_t make_page_map(CUtensorMap* m, const void* base, int d, int hkv, int 
 
 template <int D>
 cudaError_t launch_d(const AttnParams& p, int grid, int num_pages, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // The shared-memory limit is an attribute of the kernel in the current
+  // device's context: set on every launch (a host-side call of a few
+  // microseconds), so a second device, or a context created anew, gets it too.
+  cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
   CUtensorMap mk, mv;
   memset(&mk, 0, sizeof mk);
   memset(&mv, 0, sizeof mv);
   if (num_pages > 0) {
-    cudaError_t e = make_page_map(&mk, p.k, D, p.hkv, num_pages, false);
+    e = make_page_map(&mk, p.k, D, p.hkv, num_pages, false);
     if (e != cudaSuccess) return e;
     e = make_page_map(&mv, p.v, D, p.hkv, num_pages, true);
     if (e != cudaSuccess) return e;
