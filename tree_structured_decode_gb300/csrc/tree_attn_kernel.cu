@@ -716,20 +716,28 @@ __device__ __forceinline__ void write_row_cols(const AttnParams& p, const UnitDe
   if (gt.pbase < 0) {
     float* dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
     if (with_lse && p.lse) p.lse[(size_t)gt.tok * p.hq + h] = lse2 * kLn2;
+    // 32-byte stores: one per sector
 #pragma unroll
-    for (int c = 0; c < N; c += 4)
-      *reinterpret_cast<float4*>(dst + c0 + c) =
-          make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+    for (int c = 0; c < N; c += 8)
+      ptx::st_global_v8(dst + c0 + c, __float_as_uint(o[c] * inv), __float_as_uint(o[c + 1] * inv),
+                        __float_as_uint(o[c + 2] * inv), __float_as_uint(o[c + 3] * inv),
+                        __float_as_uint(o[c + 4] * inv), __float_as_uint(o[c + 5] * inv),
+                        __float_as_uint(o[c + 6] * inv), __float_as_uint(o[c + 7] * inv));
   } else {
     const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
     uint16_t* dst = p.part_o + slot * D;
 #pragma unroll
     for (int c = 0; c < N; c += 2) amax = ptx::max3(amax, fabsf(o[c]), fabsf(o[c + 1]));
 #pragma unroll
-    for (int c = 0; c < N; c += 8)
-      *reinterpret_cast<uint4*>(dst + c0 + c) =
-          make_uint4(ptx::pack_f16(o[c] * inv, o[c + 1] * inv), ptx::pack_f16(o[c + 2] * inv, o[c + 3] * inv),
-                     ptx::pack_f16(o[c + 4] * inv, o[c + 5] * inv), ptx::pack_f16(o[c + 6] * inv, o[c + 7] * inv));
+    for (int c = 0; c < N; c += 16)
+      ptx::st_global_v8(dst + c0 + c, ptx::pack_f16(o[c] * inv, o[c + 1] * inv),
+                        ptx::pack_f16(o[c + 2] * inv, o[c + 3] * inv),
+                        ptx::pack_f16(o[c + 4] * inv, o[c + 5] * inv),
+                        ptx::pack_f16(o[c + 6] * inv, o[c + 7] * inv),
+                        ptx::pack_f16(o[c + 8] * inv, o[c + 9] * inv),
+                        ptx::pack_f16(o[c + 10] * inv, o[c + 11] * inv),
+                        ptx::pack_f16(o[c + 12] * inv, o[c + 13] * inv),
+                        ptx::pack_f16(o[c + 14] * inv, o[c + 15] * inv));
   }
 }
 
