@@ -465,6 +465,32 @@ def bench_ours(args, rank, world, local):
             del rr
             torch.cuda.empty_cache()
 
+    # ---- plan ablation on this workload (the pages' "greedy grouping"
+    # against fixed edge assignments, and the latency model against the
+    # pages' cost proxy)
+    ablation = {}
+    if not args.no_ablation and args.edges == "greedy" and not args.plan_opts:
+        variants = (("greedy_latency_model", {}), ("greedy_pages_proxy", {"cost_model": 1}),
+                    ("every_edge_0", {"force_edges": np.zeros(spec.n_nodes, dtype=np.int8)}),
+                    ("every_edge_1", {"force_edges": np.ones(spec.n_nodes, dtype=np.int8)}))
+        for name, opts2 in variants:
+            rr = bench_workload(args.workload, dev, flush, stream, args.per_workload_steps,
+                                min(args.warmup, 5), opts2)
+            ablation[name] = {"ms_per_step": round(float(np.mean(rr["step_ms"])), 5),
+                              "kernel_ms": round(float(np.mean(rr["part_ms"])), 5),
+                              "merge_ms": round(float(np.mean(rr["merge_ms"])), 5),
+                              "n_units": rr["stats"]["n_units"],
+                              "n_partials": rr["stats"]["n_partials"],
+                              "group_kv_tokens": rr["stats"]["group_kv_tokens"],
+                              "device_status": rr["device_status"]}
+            rr["plan"].close()
+            del rr
+            torch.cuda.empty_cache()
+        best_fixed = min(ablation["every_edge_0"]["ms_per_step"], ablation["every_edge_1"]["ms_per_step"])
+        ablation["greedy_speedup_over_best_fixed"] = round(
+            best_fixed / ablation["greedy_latency_model"]["ms_per_step"], 3)
+        ablation["steps_each"] = args.per_workload_steps
+
     line = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step, 5),
@@ -488,6 +514,7 @@ def bench_ours(args, rank, world, local):
         "clocks": clocks.result() if clocks.ok else None,
         "device_status": r["device_status"],
         "per_workload": per,
+        "plan_ablation": ablation,
     }
     if line["clocks"] is None:  # NVML unavailable: nvidia-smi over a repeat of the steps
         with ClockSampler(local) as clk:
@@ -604,6 +631,7 @@ def main():
     ap.add_argument("--workload", default="irreg", choices=sorted(W.CONFIGS))
     ap.add_argument("--per-workload-steps", type=int, default=20)
     ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single-core-sample", default=None, help=argparse.SUPPRESS)

@@ -75,7 +75,9 @@ typedef enum {
  * a NULL options pointer means all defaults. */
 typedef struct {
   int64_t gamma;            /* [64] weight of an intermediate result per row
-                               (the cost model's SplitKVCost_R = gamma*nQ*d) */
+                               (the cost model's SplitKVCost_R = gamma*nQ*d;
+                               gamma, beta, ts_q_set and ts_c act with
+                               cost_model = 1)                               */
   int64_t beta;             /* [0] optional weight of KV duplicated by a join */
   int32_t ts_q_set[4];      /* [16,64,128] query tile sizes of the cost model;
                                zero entries end the list                     */
@@ -112,6 +114,15 @@ typedef struct {
   int32_t no_pack;          /* [0] 1: never pack thin groups (up to four
                                short groups of one kv head sharing a unit,
                                one page of each per KV tile)                 */
+  int32_t cost_model;       /* [0] the cost the planner minimises.  0: a
+                               latency model with per-tile, per-unit and
+                               per-partial times measured on GB300 (the
+                               FastTree review page's objective, "问题形式化",
+                               is the plan's latency), used for the edge
+                               decisions and the CTA schedule; 1: the pages'
+                               padding-and-intermediate-result proxy
+                               ("开销模型": gamma, beta, ts_q_set, ts_c).  The
+                               chunk length follows split_waves either way */
 } tree_attn_options;
 
 /* Sizes of a plan, for logging and roofline accounting. */

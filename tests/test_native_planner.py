@@ -31,6 +31,9 @@ def _native(spec, **opt):
         return p.describe(), p.stats(), p.schedule()
 
 
+PROXY = 1  # cost_model: the pages' padding-and-intermediate-result proxy
+
+
 def _reference(spec, **opt):
     o = P.PlannerOptions()
     for k in ("gamma", "beta", "ts_c", "mma_min_rows", "force_path"):
@@ -63,6 +66,8 @@ def _check_chunks(got):
 
 
 def _same(spec, **opt):
+    # the pages' cost model: decisions compared with the reference planner
+    opt.setdefault("cost_model", PROXY)
     got, stats, sched = _native(spec, **opt)
     ref = _reference(spec, **opt)
     assert got["edges"] == ref["edges"]
@@ -78,6 +83,10 @@ def _same(spec, **opt):
     assert stats["n_groups"] == len(ref["groups"])
     assert stats["n_units"] == len(sched["units"]) // 8
     check_schedule(spec, sched, num_sms=opt["num_sms"] if "num_sms" in opt else 152)
+    # the default (measured latency) model: another plan, the same invariants
+    lat = {k: v for k, v in opt.items() if k != "cost_model"}
+    _, _, sched_lat = _native(spec, **lat)
+    check_schedule(spec, sched_lat, num_sms=lat.get("num_sms", 152))
     return got, stats, sched
 
 
@@ -207,3 +216,35 @@ def test_schedule_check_catches_a_planted_fault():
     for f in faults:
         with pytest.raises(AssertionError):
             check_schedule(spec, f)
+
+
+def _edge_of_child(lens, rows_root, rows_child, **opt):
+    # root 0 with one child 1; GQA 1, one kv head; rows_root - rows_child
+    # query tokens of the root itself, rows_child of the child
+    qnode = [0] * (rows_root - rows_child) + [1] * rows_child
+    qend = [lens[0]] * (rows_root - rows_child) + [lens[1]] * rows_child
+    spec = W._finish("edge", [-1, 0], lens, qnode, qend, 1, 1, 128, seed=1)
+    got, _, sched = _native(spec, **opt)
+    check_schedule(spec, sched)
+    return got["edges"][1]
+
+
+def test_latency_model_decisions_worked_by_hand():
+    # Latency model, in thousandths of one KV tile's time: a 128-row query
+    # tile over len tokens costs ceil(len / 64) * 1000 + 8200 (its unit's
+    # start-up and epilogue); a thin group (<= 32 rows, <= 128 tokens) a
+    # quarter of ceil(len / 16) * 1000 + 8200 (four share a unit); an extra
+    # partial 29 per row.
+    # Root 2048 tokens with 250 rows, child 64 tokens with 100 of them:
+    #   C0 = 2 * (32000 + 8200) + (1000 + 8200) + 29 * 100 = 92500
+    #   C1 = 2 * (32000 + 8200) + (33000 + 8200)            = 121600  -> edge 0
+    assert _edge_of_child([2048, 64], 250, 100) == 0
+    # Root 64 tokens with 140 rows, child 64 tokens with 12 (a thin group):
+    #   C0 = 2 * (1000 + 8200) + (4 * 1000 + 8200) / 4 + 29 * 12 = 21798
+    #   C1 = 1 * (1000 + 8200) + (8 * 1000 + 8200) / 4            = 13250  -> edge 1
+    assert _edge_of_child([64, 64], 140, 12) == 1
+    # the pages' proxy on the same trees (d = 128, gamma = 64), by hand:
+    #   first:  C0 = (6*2048 + 28*64 + 64*100) d = 20480 d < C1 = (106*2048 + 28*2112) d
+    #   second: C0 = (116*64 + 4*64 + 64*12) d = 8448 d >= C1 = (4*128) d = 512 d
+    assert _edge_of_child([2048, 64], 250, 100, cost_model=PROXY) == 0
+    assert _edge_of_child([64, 64], 140, 12, cost_model=PROXY) == 1

@@ -50,6 +50,7 @@ class Options(ctypes.Structure):
         ("debug_stuck_wait", ctypes.c_int32),
         ("merge_mode", ctypes.c_int32),
         ("no_pack", ctypes.c_int32),
+        ("cost_model", ctypes.c_int32),
     ]
 
 

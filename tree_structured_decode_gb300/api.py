@@ -17,7 +17,7 @@ from ._abi import Options, PlanStats, check, load_library
 _OPTION_KEYS = {
     "gamma", "beta", "ts_q_set", "ts_c", "mma_min_rows", "split_tokens",
     "min_split_tokens", "split_waves", "num_sms", "force_path", "host_only",
-    "wait_timeout_us", "force_edges", "debug_stuck_wait", "merge_mode", "no_pack",
+    "wait_timeout_us", "force_edges", "debug_stuck_wait", "merge_mode", "no_pack", "cost_model",
 }
 
 

@@ -22,6 +22,8 @@ inline int64_t pad(int64_t ts, int64_t n) {
 struct CostModel {
   const Options& o;
   int64_t d;
+  int64_t hkv;
+  int r;
   int64_t ts_q(int64_t n) const {
     int64_t best = -1, mx = 0;
     for (int32_t t : o.ts_q) {
@@ -36,14 +38,28 @@ struct CostModel {
   int64_t pc(int64_t nq, int64_t len) const {
     return nq * pad(o.ts_c, std::min<int64_t>(len, o.ts_c)) * d;
   }
+  // Latency of one kv head's share of a group of n rows over len tokens
+  // (latency model): tensor-core query tiles of 128 rows, each streaming
+  // the span in 64-token tiles as one unit; thin groups (at most one warp's
+  // 32 rows) share a unit four ways, one page of each per tile.
+  int64_t lat_group(int64_t n, int64_t len) const {
+    if (n <= 0) return 0;
+    if (!o.no_pack && n <= kPackMmaRows && kPackMmaRows % r == 0 &&
+        (len <= (int64_t)kPackMaxBlocks * kPageSize || hkv % kPackSlots == 0))
+      return (ceil_div(len, kPageSize) * kLatTile + kLatUnit) / kPackSlots;
+    return ceil_div(n, kMmaTileRows) * (ceil_div(len, kKvTileTokens) * kLatTile + kLatUnit);
+  }
   // C_0: l keeps its own group; its rows also stay in v's (two partials).
   int64_t split_kv(int64_t nq_curr, int64_t nq_l, int64_t len_l, int64_t len_v) const {
+    if (o.cost_model == 0)
+      return lat_group(nq_curr, len_v) + lat_group(nq_l, len_l) + kLatMergeRow * nq_l;
     return pq(nq_curr, len_v) + pc(nq_curr, len_v) + pq(nq_l, len_l) +
            pc(nq_l, len_l) + o.gamma * nq_l * d;
   }
   // C_1: l joins v; l's group carries v's KV and takes l's rows.
   int64_t split_q(int64_t nq_curr, int64_t nq_l, int64_t len_l, int64_t len_v) const {
     int64_t rest = nq_curr - nq_l;
+    if (o.cost_model == 0) return lat_group(rest, len_v) + lat_group(nq_l, len_l + len_v);
     int64_t c = pq(rest, len_v) + pc(rest, len_v) + pq(nq_l, len_l + len_v) +
                 pc(nq_l, len_l + len_v);
     if (rest > 0) c += o.beta * len_v * d;
@@ -182,7 +198,7 @@ tree_attn_status build_host_plan(
   for (int i = n - 1; i >= 1; --i) A[parent[bfs[i]]] += A[bfs[i]];
 
   // ------------------------------------------ Algorithm 1 (greedy, BFS)
-  CostModel cm{p.opt, d};
+  CostModel cm{p.opt, d, hkv, r};
   p.L.assign(n, 0);
   for (int v = 0; v < n; ++v) p.L[v] = node_kv_len[v];
   p.edge.assign(n, 0);
@@ -549,9 +565,14 @@ tree_attn_status build_host_plan(
   {
     std::vector<int32_t> order(nu);
     for (int64_t i = 0; i < nu; ++i) order[i] = (int32_t)i;
-    // blocks streamed plus a fixed start-up and epilogue cost per unit
+    // blocks streamed plus a fixed start-up and epilogue cost per unit (the
+    // latency model: its measured per-tile and per-unit times)
     auto cost = [&](int32_t i) {
-      return (int64_t)(p.units[i].blk1 - p.units[i].blk0) + ((p.units[i].path & kPathMma) ? 6 : 3);
+      const int64_t nb = p.units[i].blk1 - p.units[i].blk0;
+      if (opt.cost_model == 0)
+        return (p.units[i].path & kPathMma) ? ceil_div(nb, kBlocksPerTile) * kLatTile + kLatUnit
+                                            : (nb + 3) * kLatTile / kBlocksPerTile;
+      return nb + ((p.units[i].path & kPathMma) ? 6 : 3);
     };
     std::stable_sort(order.begin(), order.end(),
                      [&](int32_t a, int32_t b) { return cost(a) > cost(b); });

@@ -59,7 +59,19 @@ struct Options {
   int32_t debug_stuck_wait = 0;
   int32_t merge_mode = 0;  // 0 separate merge kernel, 1 fused into the partial kernel
   int32_t no_pack = 0;     // 1: never pack thin groups
+  int32_t cost_model = 0;  // 0: the measured latency model, 1: the pages' padding proxy
 };
+
+// Measured latency model (the plan objective Latency(Groups(VT(T, f))) of
+// the FastTree review page, "问题形式化", with costs measured on GB300).
+// Times in thousandths of the period of one 64-token KV tile on a CTA, fitted
+// to per-CTA timelines of the partial-attention kernel: a work unit costs
+// kLatTile per KV tile plus kLatUnit of start-up and epilogue (the same for
+// 64- and 128-row tiles), and a query row's extra partial result costs
+// kLatMergeRow (written by the kernel, folded by the merge pass).
+constexpr int64_t kLatTile = 1000;
+constexpr int64_t kLatUnit = 8200;
+constexpr int64_t kLatMergeRow = 29;
 
 // One work unit as the kernels read it (32 bytes, device POD).
 struct UnitDesc {

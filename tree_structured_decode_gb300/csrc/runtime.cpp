@@ -50,6 +50,7 @@ ta::Options to_options(const tree_attn_options* o) {
   r.debug_stuck_wait = o->debug_stuck_wait;
   r.merge_mode = o->merge_mode;
   r.no_pack = o->no_pack;
+  r.cost_model = o->cost_model;
   return r;
 }
 
