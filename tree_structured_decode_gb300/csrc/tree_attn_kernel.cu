@@ -79,7 +79,8 @@ struct Cfg {
   static constexpr int kOffML = kOffBar + kNumBars * 8 + 16;  // float [4][8][2]
   // the dynamic shared window starts 1024-byte aligned (checked at start)
   static constexpr int kSmem = kOffML + 4 * kSimtTileRows * 2 * 4;
-  static_assert(kSmem <= 115 * 1024, "two CTAs per SM must fit in shared memory");
+  // two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+  static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM must fit in shared memory");
   // scratch of the CUDA-core path, where its four warps' O are combined
   static_assert(4 * kSimtTileRows * D * 4 <= kScratchBytes, "combine scratch too small");
   // A stage holds K as [64-column half][tile token][128 B] (one box per page
