@@ -32,13 +32,17 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int total = p.n_items * p.hq;
+  // The merge items are plan tables, in place before the partial-attention
+  // kernel started: this warp's first one is read before the dependency wait.
+  MergeItem it_first = {};
+  if (2 * gw + sub < total) it_first = p.items[(2 * gw + sub) / p.hq];
   // launched as a programmatic dependent of the partial-attention kernel:
   // wait here until that grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int r0 = 2 * gw; r0 < total; r0 += 2 * nw) {
     const int idx = r0 + sub;
     if (idx >= total) continue;
-    const MergeItem it = p.items[idx / p.hq];
+    const MergeItem it = r0 == 2 * gw ? it_first : p.items[idx / p.hq];
     const int h = idx % p.hq;
     const float2* ml_h = p.part_ml + (size_t)it.poff * p.hq + h;  // partial k at ml_h[k * hq]
     const uint16_t* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + l16 * EPL;  // fp16

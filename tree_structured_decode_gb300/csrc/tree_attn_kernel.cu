@@ -75,7 +75,7 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffScratch = kOffV + kStages * kTileBytes;
   static constexpr int kOffBar = kOffScratch + kScratchBytes;
-  static constexpr int kNumBars = 4 * kStages + 12;
+  static constexpr int kNumBars = 5 * kStages + 12;
   static constexpr int kOffML = kOffBar + kNumBars * 8 + 16;  // float [4][8][2]
   // the dynamic shared window starts 1024-byte aligned (checked at start)
   static constexpr int kSmem = kOffML + 4 * kSimtTileRows * 2 * 4;
@@ -119,6 +119,9 @@ struct Bars {
   __device__ uint32_t q_full(int i) const { return b + 8 * (4 * S + 8 + i); }
   __device__ uint32_t never() const { return b + 8 * (4 * S + 10); }
   __device__ uint32_t o_empty() const { return b + 8 * (4 * S + 11); }
+  // V copies of a tile with unfilled page slots land here; the V producer
+  // zeroes those slots' rows and only then completes vfull
+  __device__ uint32_t vland(int s) const { return b + 8 * (4 * S + 12 + s); }
 };
 
 // Bounded wait.  Returns false (without waiting further) once the CTA has
@@ -160,6 +163,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, long l
     if ((long long)(ptx::globaltimer() - t0) > limit_ns) return;
 }
 
+// valid slots of a tile's four pages, 5 bits a page, when every page is full
+constexpr int kFullTileValid = 16 | 16 << 5 | 16 << 10 | 16 << 15;
+
 __device__ __forceinline__ int unit_tiles(const UnitDesc& u) {
   return (u.blk1 - u.blk0 + kBpt - 1) / kBpt;
 }
@@ -178,6 +184,7 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
   uint32_t g = 0;
   if (!kIsV && p.debug_stuck_wait) warp_wait(B.never(), 0, sh, p.err, p.wait_timeout_ns);
   uint32_t filled[C::kStages];  // 1 + tile index of the last fill issued per stage
+  uint32_t land_par = 0;        // V: phase bit of each stage's vland barrier
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) filled[s] = 0;
   UnitDesc un = u0 < u1 ? p.units[u0] : UnitDesc{};
@@ -188,16 +195,29 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
       const int s = g % C::kStages;
       const int nb = min(kBpt, u.blk1 - b0);
       int page[kBpt];  // all loads in flight while waiting for the stage
+      int nvm = kFullTileValid;  // V: valid slots of the pages
 #pragma unroll
-      for (int bb = 0; bb < kBpt; ++bb) page[bb] = bb < nb ? __ldg(&p.blocks[b0 + bb].x) : 0;
+      for (int bb = 0; bb < kBpt; ++bb) {
+        if constexpr (kIsV) {
+          const int2 r = bb < nb ? __ldg(&p.blocks[b0 + bb]) : make_int2(0, 16);
+          page[bb] = r.x;
+          nvm = (nvm & ~(31 << (5 * bb))) | (r.y & 31) << (5 * bb);
+        } else {
+          page[bb] = bb < nb ? __ldg(&p.blocks[b0 + bb].x) : 0;
+        }
+      }
       const uint32_t full = kIsV ? B.vfull(s) : B.kfull(s);
+      // V pages with unfilled slots land on vland first (their rows are
+      // zeroed below); everything else lands on the stage's full barrier
+      const bool zero = kIsV && nvm != kFullTileValid;
+      const uint32_t land = zero ? B.vland(s) : full;
       if (g >= (uint32_t)C::kStages &&
           !warp_wait(kIsV ? B.vempty(s) : B.kempty(s), ((g / C::kStages) + 1) & 1, sh, p.err,
                      p.wait_timeout_ns))
         continue;
       if (warp_aborted(sh)) continue;
       const bool leader = ptx::elect_one();
-      if (leader) ptx::mbar_arrive_expect_tx(full, (uint32_t)nb * C::kBlockBytes);
+      if (leader) ptx::mbar_arrive_expect_tx(land, (uint32_t)nb * C::kBlockBytes);
       const int kvh = u.kvh, hstep = (u.path & kUnitHeads) ? 1 : 0;  // page bb's kv head
       const uint32_t dst = sh.base + (kIsV ? C::kOffV : C::kOffK) + s * C::kTileBytes;
 #pragma unroll
@@ -207,13 +227,38 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h)
               ptx::tma_load_4d(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0, kvh + bb * hstep,
-                               page[bb], full);
+                               page[bb], land);
           } else if constexpr (D == 128) {  // both 64-column halves of V in one box
-            ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, kvh + bb * hstep, page[bb], full);
+            ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, kvh + bb * hstep, page[bb], land);
           } else {
-            ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, kvh + bb * hstep, page[bb], full);
+            ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, kvh + bb * hstep, page[bb], land);
           }
         }
+      }
+      if (zero) {
+        // A page slot that holds no token may hold anything, NaN included;
+        // its P is 0 but 0 * NaN is not 0.  Zero those V rows once the
+        // copies have landed, then hand the stage to P.V.
+        const uint32_t par = (land_par >> s) & 1;
+        land_par ^= 1u << s;
+        if (warp_wait(B.vland(s), par, sh, p.err, p.wait_timeout_ns)) {
+          uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes;
+          const int lane = threadIdx.x & 31;
+#pragma unroll
+          for (int bb = 0; bb < kBpt; ++bb) {
+            const int nv = (nvm >> (5 * bb)) & 31;
+            for (int idx = lane; idx < (16 - nv) * 8 * C::kHalves; idx += 32) {
+              const int r = nv + idx / (8 * C::kHalves), hh = (idx >> 3) % C::kHalves, ch = idx & 7;
+              *reinterpret_cast<uint4*>(vst + bb * C::kBlockBytes + hh * 2048 + r * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+        } else {
+          drain_wait(B.vland(s), par, kDrainLimitNs);  // the copies land before the CTA may exit
+        }
+        __syncwarp();
+        if (ptx::elect_one()) ptx::mbar_arrive(full);
       }
 #pragma unroll
       for (int t = 0; t < C::kStages; ++t)
@@ -841,19 +886,17 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     };
     load_records(0);
     for (int j = 0; j < T; ++j) {
-      const int s = (g + j) % C::kStages;
       const int sb = (gm + j) & 1;
       const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
       // Visible columns of this row in each page of the tile (decoded while
       // QK^T may still run).  In a packed unit warp w is slot w and sees
       // only page w of every tile.
       int lim[kBpt];
-      bool partial = false, full = nb == kBpt;
+      bool full = nb == kBpt;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
         lim[bb] = 0;
         if (bb < nb) {
-          partial |= (mt[bb] & 31) < 16;
           if (row_ok && !packed) lim[bb] = max(0, min(mt[bb] & 31, vis - (mt[bb] >> 5)));
         }
         full = full && (!row_ok || lim[bb] == 16);
@@ -865,9 +908,6 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       const int lim_p = packed && row_ok && my_phase
                             ? max(0, min(mt_p & 31, vis - ((mt_p & kPosMask) >> 5)))
                             : 0;
-      int nvalid = 0;  // valid slots of the tile's pages, 5 bits each
-#pragma unroll
-      for (int bb = 0; bb < kBpt; ++bb) nvalid |= (mt[bb] & 31) << (5 * bb);
       if (j + 1 < T) load_records(j + 1);
       bool ok = wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
@@ -909,8 +949,6 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         }
         lsum = (e4[0] + e4[1]) + (e4[2] + e4[3]);
       } else {
-        // a warp whose rows all see the whole tile skips the masks
-        const bool fast = __all_sync(0xffffffffu, full);
         float sv[kTileTok];
         if (ok && wact) {
 #pragma unroll
@@ -925,24 +963,28 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 #pragma unroll
           for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
         }
-        // row max over the visible columns; masked scores select -inf
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (fast) {
+        // Scores this row may not see become -inf (exp2 then gives exactly
+        // 0); a warp whose rows all see the whole tile skips the selects.
+        // One exponentiation body then serves every tile, which keeps the
+        // compute warps' loop short.
+        if (!__all_sync(0xffffffffu, full)) {
 #pragma unroll
-          for (int c = 0; c < kTileTok; c += 2)
-            m4[(c >> 1) & 3] = ptx::max3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < kTileTok; ++c)
-            m4[c & 3] = fmaxf(m4[c & 3], (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY);
+          for (int c = 0; c < kTileTok; ++c) sv[c] = (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY;
         }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kTileTok; c += 2)
+          m4[(c >> 1) & 3] = ptx::max3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
         const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
         if (wact && mx > m_run + kRescaleLog2) {
           m_new = mx;
           alpha = ptx::ex2(m_run - m_new);
         }
-        if (wact && fast) {
-          const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(-m_new, -m_new);
+        if (wact) {
+          // a row that has seen no key yet has only -inf scores here: any
+          // finite offset keeps their exponentials at 0 (and not NaN)
+          const float nm = m_new == -INFINITY ? 0.f : -m_new;
+          const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(nm, nm);
           uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // (0.f, 0.f) pairs
 #pragma unroll
           for (int c = 0; c < kTileTok; c += 2) {
@@ -956,18 +998,6 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 #pragma unroll
           for (int k = 0; k < 4; ++k) ptx::f2_split(acc[k], e8[2 * k], e8[2 * k + 1]);
           lsum = ((e8[0] + e8[1]) + (e8[2] + e8[3])) + ((e8[4] + e8[5]) + (e8[6] + e8[7]));
-        } else if (wact) {
-          float e4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int c = 0; c < kTileTok; c += 2) {
-            const float xa = (c & 15) < lim[c >> 4] ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY;
-            const float xb =
-                ((c + 1) & 15) < lim[(c + 1) >> 4] ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY;
-            const float a = ptx::ex2(xa), b = ptx::ex2(xb);
-            pk[c >> 1] = ptx::pack_bf16(a, b);
-            e4[(c >> 1) & 3] += a + b;
-          }
-          lsum = (e4[0] + e4[1]) + (e4[2] + e4[3]);
         }
       }
       l_run = fmaf(l_run, alpha, lsum);
@@ -1003,22 +1033,6 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         }
         ptx::tmem_wait_st();
       }
-      if (partial &&
-          wait_bar(B.vfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns)) {
-        // zero the V rows of page slots that hold no token (they may hold
-        // anything; P is 0 there but 0 * NaN is not 0)
-        uint8_t* vst = sh.ptr + C::kOffV + s * C::kTileBytes;
-#pragma unroll
-        for (int bb = 0; bb < kBpt; ++bb) {
-          const int nv = (nvalid >> (5 * bb)) & 31;
-          for (int idx = tid; idx < (16 - nv) * 8 * C::kHalves; idx += kComputeThreads) {
-            const int r = nv + idx / (8 * C::kHalves), hh = (idx >> 3) % C::kHalves, ch = idx & 7;
-            *reinterpret_cast<uint4*>(vst + bb * C::kBlockBytes + hh * 2048 + r * 128 + ch * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
-      }
-      if (partial) ptx::fence_proxy_async_smem();  // the zeroed V rows
       ptx::tc_fence_before();
       ptx::mbar_arrive(B.p_full(sb));
     }
@@ -1098,6 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       ptx::mbar_init(B.kempty(s), 1);
       ptx::mbar_init(B.vfull(s), 1);
       ptx::mbar_init(B.vempty(s), 1);
+      ptx::mbar_init(B.vland(s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(B.s_full(i), 1);
