@@ -39,6 +39,8 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#include <type_traits>
+
 namespace ta {
 namespace {
 
@@ -812,6 +814,22 @@ __device__ __noinline__ void rewrite_scaled_partial(const AttnParams& p, const U
   }
 }
 
+// O *= alpha for this thread's row (a lazy rescale: rare, so out of line,
+// which keeps the tile loop short)
+template <int D>
+__device__ __noinline__ void rescale_o(uint32_t o_tmem, float alpha) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    float t32[32];
+    ptx::tmem_ld32(o_tmem + c * 32, t32);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) t32[e] *= alpha;
+    ptx::tmem_st32(o_tmem + c * 32, t32);
+  }
+  ptx::tmem_wait_st();
+}
+
 // The four compute warps: thread i owns TMEM lane / query row i.
 template <int D>
 __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared& sh,
@@ -872,7 +890,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     const QRow q_next = nxt >= 0 ? q_row<D>(p, nxt, tid) : QRow{GroupTok{-1, 0, -1, 0}, p.q};
     const bool row_ok = tid < u.nrows && gt_row.tok >= 0;
     const bool wact = warp * 32 < u.nrows;  // warps of padding rows keep the barriers only
-    const bool packed = gt_row.slot() >= 0;  // warp w holds slot w's rows
+    const bool packed = gt_row.slot() >= 0;  // warp w holds slot w's rows (same in a warp)
     float m_run = -INFINITY, l_run = 0.f;
     // the tiles' page records (span position * 32 + valid slots), each
     // loaded one tile ahead; packed tiles always hold kBpt pages
@@ -885,157 +903,157 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       mt_p = packed ? __ldg(&blk[warp].y) : 0;
     };
     load_records(0);
-    for (int j = 0; j < T; ++j) {
-      const int sb = (gm + j) & 1;
-      const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
-      // Visible columns of this row in each page of the tile (decoded while
-      // QK^T may still run).  In a packed unit warp w is slot w and sees
-      // only page w of every tile.
-      int lim[kBpt];
-      bool full = nb == kBpt;
+    // The tile loop in two forms, packed units' and the others', each
+    // compiled on its own: the loop a unit runs holds only its own form.
+    auto tile_loop = [&](auto packed_c) {
+      constexpr bool kPacked = decltype(packed_c)::value;
+      for (int j = 0; j < T; ++j) {
+        const int sb = (gm + j) & 1;
+        const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
+        // Visible columns of this row in each page of the tile (decoded while
+        // QK^T may still run).  In a packed unit warp w is slot w and sees
+        // only page w of every tile.
+        int lim[kBpt];
+        bool full = nb == kBpt;
 #pragma unroll
-      for (int bb = 0; bb < kBpt; ++bb) {
-        lim[bb] = 0;
-        if (bb < nb) {
-          if (row_ok && !packed) lim[bb] = max(0, min(mt[bb] & 31, vis - (mt[bb] >> 5)));
-        }
-        full = full && (!row_ok || lim[bb] == 16);
-      }
-      // in a unit packed in two phases a row sees only its phase's tiles
-      // (phase 0 in lanes 0-15, phase 1 in lanes 16-31 of each slot)
-      const bool my_phase =
-          !(u.path & kUnitPhases) || ((mt_p >> kPhaseShift) & 1) == ((tid & 31) >> 4);
-      const int lim_p = packed && row_ok && my_phase
-                            ? max(0, min(mt_p & 31, vis - ((mt_p & kPosMask) >> 5)))
-                            : 0;
-      if (j + 1 < T) load_records(j + 1);
-      bool ok = wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      ptx::tc_fence_after();
-      // every QK^T of this unit has completed once the last S is ready: the
-      // query buffer is free, so the next unit's query tile starts streaming
-      if (j == T - 1 && nxt >= 0) {
-        load_q<D>(q_next, qbuf, tid);
-        gt_next = q_next.gt;
-      }
-      float m_new = m_run, alpha = 1.f, lsum = 0.f;
-      uint32_t pk[kTileTok / 2];
-      // P rounds to bf16 for the tensor cores; the row sum is kept exact in
-      // fp32 and normalises both O and the lse.
-      if (packed) {
-        float sv[16];
-        if (ok && wact) {
-          ptx::tmem_ld16(tmem + lane_base + sb * kTileTok + warp * 16, sv);
-          ptx::tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 16; ++c) sv[c] = 0.f;
-        }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < 16; ++c) m4[c & 3] = fmaxf(m4[c & 3], c < lim_p ? sv[c] : -INFINITY);
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
-        if (wact && mx > m_run + kRescaleLog2) {
-          m_new = mx;
-          alpha = ptx::ex2(m_run - m_new);
-        }
-        float e4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < 16; c += 2) {
-          const float a = ptx::ex2(c < lim_p ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY);
-          const float b = ptx::ex2(c + 1 < lim_p ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY);
-          pk[c >> 1] = ptx::pack_bf16(a, b);
-          e4[(c >> 1) & 3] += a + b;
-        }
-        lsum = (e4[0] + e4[1]) + (e4[2] + e4[3]);
-      } else {
-        float sv[kTileTok];
-        if (ok && wact) {
-#pragma unroll
-          for (int c = 0; c < kTileTok / 32; ++c) {
-            float t32[32];
-            ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + c * 32, t32);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t32[e];
+        for (int bb = 0; bb < kBpt; ++bb) {
+          lim[bb] = 0;
+          if (bb < nb) {
+            if (row_ok && !kPacked) lim[bb] = max(0, min(mt[bb] & 31, vis - (mt[bb] >> 5)));
           }
-          ptx::tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
+          full = full && (!row_ok || lim[bb] == 16);
         }
-        // Scores this row may not see become -inf (exp2 then gives exactly
-        // 0); a warp whose rows all see the whole tile skips the selects.
-        // One exponentiation body then serves every tile, which keeps the
-        // compute warps' loop short.
-        if (!__all_sync(0xffffffffu, full)) {
-#pragma unroll
-          for (int c = 0; c < kTileTok; ++c) sv[c] = (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY;
-        }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < kTileTok; c += 2)
-          m4[(c >> 1) & 3] = ptx::max3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
-        if (wact && mx > m_run + kRescaleLog2) {
-          m_new = mx;
-          alpha = ptx::ex2(m_run - m_new);
-        }
-        if (wact) {
-          // a row that has seen no key yet has only -inf scores here: any
-          // finite offset keeps their exponentials at 0 (and not NaN)
-          const float nm = m_new == -INFINITY ? 0.f : -m_new;
-          const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(nm, nm);
-          uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // (0.f, 0.f) pairs
-#pragma unroll
-          for (int c = 0; c < kTileTok; c += 2) {
-            float xa, xb;
-            ptx::f2_split(ptx::fma_f32x2(ptx::f2(sv[c], sv[c + 1]), sc2, nm2), xa, xb);
-            const float a = ptx::ex2(xa), b = ptx::ex2(xb);
-            pk[c >> 1] = ptx::pack_bf16(a, b);
-            acc[(c >> 1) & 3] = ptx::add_f32x2(acc[(c >> 1) & 3], ptx::f2(a, b));
-          }
-          float e8[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) ptx::f2_split(acc[k], e8[2 * k], e8[2 * k + 1]);
-          lsum = ((e8[0] + e8[1]) + (e8[2] + e8[3])) + ((e8[4] + e8[5]) + (e8[6] + e8[7]));
-        }
-      }
-      l_run = fmaf(l_run, alpha, lsum);
-      m_run = m_new;
-      // a rescale of O waits until O holds the previous tile's P.V
-      if (ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f) &&
-          __all_sync(0xffffffffu, wait_bar(B.pv_done((gm + j - 1) & 1), ((gm + j - 1) >> 1) & 1, sh,
-                                           p.err, p.wait_timeout_ns))) {
+        // in a unit packed in two phases a row sees only its phase's tiles
+        // (phase 0 in lanes 0-15, phase 1 in lanes 16-31 of each slot)
+        const bool my_phase =
+            !(u.path & kUnitPhases) || ((mt_p >> kPhaseShift) & 1) == ((tid & 31) >> 4);
+        const int lim_p = kPacked && row_ok && my_phase
+                              ? max(0, min(mt_p & 31, vis - ((mt_p & kPosMask) >> 5)))
+                              : 0;
+        if (j + 1 < T) load_records(j + 1);
+        bool ok = wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
+        ok = __all_sync(0xffffffffu, ok);
         ptx::tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float t32[32];
-          ptx::tmem_ld32(o_tmem + c * 32, t32);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) t32[e] *= alpha;
-          ptx::tmem_st32(o_tmem + c * 32, t32);
+        // every QK^T of this unit has completed once the last S is ready: the
+        // query buffer is free, so the next unit's query tile starts streaming
+        if (j == T - 1 && nxt >= 0) {
+          load_q<D>(q_next, qbuf, tid);
+          gt_next = q_next.gt;
         }
-        ptx::tmem_wait_st();
-      }
-      // P (bf16 pairs, 32 columns) replaces S in the first half of its TMEM
-      // buffer; the S values were read above
-      if (ok && wact) {
-        const uint32_t pt = tmem + lane_base + sb * kTileTok;
-        if (packed) {
-          // this warp's page is P columns [8w, 8w + 8); the rest is zero
-          uint32_t pw[kTileTok / 2];
+        float m_new = m_run, alpha = 1.f, lsum = 0.f;
+        uint32_t pk[kTileTok / 2];
+        // P rounds to bf16 for the tensor cores; the row sum is kept exact in
+        // fp32 and normalises both O and the lse.
+        if constexpr (kPacked) {
+          float sv[16];
+          if (ok && wact) {
+            ptx::tmem_ld16(tmem + lane_base + sb * kTileTok + warp * 16, sv);
+            ptx::tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int c = 0; c < kTileTok / 2; ++c) pw[c] = (c >> 3) == warp ? pk[c & 7] : 0u;
-          ptx::tmem_st32u(pt, pw);
+            for (int c = 0; c < 16; ++c) sv[c] = 0.f;
+          }
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < 16; ++c) m4[c & 3] = fmaxf(m4[c & 3], c < lim_p ? sv[c] : -INFINITY);
+          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+          if (wact && mx > m_run + kRescaleLog2) {
+            m_new = mx;
+            alpha = ptx::ex2(m_run - m_new);
+          }
+          float e4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < 16; c += 2) {
+            const float a = ptx::ex2(c < lim_p ? fmaf(sv[c], p.scale_log2, -m_new) : -INFINITY);
+            const float b = ptx::ex2(c + 1 < lim_p ? fmaf(sv[c + 1], p.scale_log2, -m_new) : -INFINITY);
+            pk[c >> 1] = ptx::pack_bf16(a, b);
+            e4[(c >> 1) & 3] += a + b;
+          }
+          lsum = (e4[0] + e4[1]) + (e4[2] + e4[3]);
         } else {
-          ptx::tmem_st32u(pt, pk);
+          float sv[kTileTok];
+          if (ok && wact) {
+#pragma unroll
+            for (int c = 0; c < kTileTok / 32; ++c) {
+              float t32[32];
+              ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + c * 32, t32);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) sv[c * 32 + e] = t32[e];
+            }
+            ptx::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < kTileTok; ++c) sv[c] = 0.f;
+          }
+          // Scores this row may not see become -inf (exp2 then gives exactly
+          // 0); a warp whose rows all see the whole tile skips the selects.
+          // One exponentiation body then serves every tile, which keeps the
+          // compute warps' loop short.
+          if (!__all_sync(0xffffffffu, full)) {
+#pragma unroll
+            for (int c = 0; c < kTileTok; ++c) sv[c] = (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY;
+          }
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < kTileTok; c += 2)
+            m4[(c >> 1) & 3] = ptx::max3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
+          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+          if (wact && mx > m_run + kRescaleLog2) {
+            m_new = mx;
+            alpha = ptx::ex2(m_run - m_new);
+          }
+          if (wact) {
+            // a row that has seen no key yet has only -inf scores here: any
+            // finite offset keeps their exponentials at 0 (and not NaN)
+            const float nm = m_new == -INFINITY ? 0.f : -m_new;
+            const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(nm, nm);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // (0.f, 0.f) pairs
+#pragma unroll
+            for (int c = 0; c < kTileTok; c += 2) {
+              float xa, xb;
+              ptx::f2_split(ptx::fma_f32x2(ptx::f2(sv[c], sv[c + 1]), sc2, nm2), xa, xb);
+              const float a = ptx::ex2(xa), b = ptx::ex2(xb);
+              pk[c >> 1] = ptx::pack_bf16(a, b);
+              acc[(c >> 1) & 3] = ptx::add_f32x2(acc[(c >> 1) & 3], ptx::f2(a, b));
+            }
+            float e8[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ptx::f2_split(acc[k], e8[2 * k], e8[2 * k + 1]);
+            lsum = ((e8[0] + e8[1]) + (e8[2] + e8[3])) + ((e8[4] + e8[5]) + (e8[6] + e8[7]));
+          }
         }
-        ptx::tmem_wait_st();
+        l_run = fmaf(l_run, alpha, lsum);
+        m_run = m_new;
+        // a rescale of O waits until O holds the previous tile's P.V
+        if (ok && wact && j > 0 && __any_sync(0xffffffffu, alpha != 1.f) &&
+            __all_sync(0xffffffffu, wait_bar(B.pv_done((gm + j - 1) & 1), ((gm + j - 1) >> 1) & 1, sh,
+                                             p.err, p.wait_timeout_ns))) {
+          ptx::tc_fence_after();
+          rescale_o<D>(o_tmem, alpha);
+        }
+        // P (bf16 pairs, 32 columns) replaces S in the first half of its TMEM
+        // buffer; the S values were read above
+        if (ok && wact) {
+          const uint32_t pt = tmem + lane_base + sb * kTileTok;
+          if constexpr (kPacked) {
+            // this warp's page is P columns [8w, 8w + 8); the rest is zero
+            uint32_t pw[kTileTok / 2];
+#pragma unroll
+            for (int c = 0; c < kTileTok / 2; ++c) pw[c] = (c >> 3) == warp ? pk[c & 7] : 0u;
+            ptx::tmem_st32u(pt, pw);
+          } else {
+            ptx::tmem_st32u(pt, pk);
+          }
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(B.p_full(sb));
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(B.p_full(sb));
-    }
+    };
+    if (packed)
+      tile_loop(std::true_type{});
+    else
+      tile_loop(std::false_type{});
     // hand the next unit's query tile to the MMA issuer, so its first QK^T
     // overlaps this unit's epilogue
     if (nxt >= 0) {
