@@ -130,29 +130,39 @@ struct Bars {
 // aborted; a wait that exceeds the limit aborts the CTA and records the
 // error.  A phase that has already completed returns true at once: every
 // issue after a wait checks the abort flag itself.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Shared& sh,
-                                         int32_t* err, long long limit_ns) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  if (*sh.abort_flag) return false;
+// The polling loop sits out of line: every wait site stays one try_wait and
+// a call, which keeps the loops that wait short.  One copy per register
+// split (0: compute warps, 1: the issuing warps), as a call must match its
+// caller's register count.
+template <int kRole>
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int32_t* err, long long limit_ns) {
+  if (*abort_flag) return false;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((n & 15) == 0) {
-      if (*sh.abort_flag) return false;
+      if (*abort_flag) return false;
       if ((long long)(ptx::globaltimer() - t0) > limit_ns) {
-        *sh.abort_flag = 1;
+        *abort_flag = 1;
         atomicCAS(err, 0, TA_DEVERR_TIMEOUT);
         return false;
       }
     }
   }
 }
+template <int kRole = 0>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Shared& sh,
+                                         int32_t* err, long long limit_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow<kRole>(bar, parity, sh.abort_flag, err, limit_ns);
+}
 
 // wait_bar for a whole (converged) warp: true only if every lane's wait
 // succeeded, so the warp stays converged.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Shared& sh,
                                           int32_t* err, long long limit_ns) {
-  return __all_sync(0xffffffffu, wait_bar(bar, parity, sh, err, limit_ns));
+  return __all_sync(0xffffffffu, wait_bar<1>(bar, parity, sh, err, limit_ns));
 }
 __device__ __forceinline__ bool warp_aborted(const Shared& sh) {
   return __any_sync(0xffffffffu, *sh.abort_flag != 0);
