@@ -331,31 +331,34 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
         ptx::mma_commit(B.pv_done(pb));
       }
     };
-    for (int j = 0; j < T; ++j) {
-      const int s = (g + j) % C::kStages;
-      const int sb = (gm + j) & 1;
-      bool ok = qok && warp_wait(B.kfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
-      // S buffer sb holds P of the tile two back until that P.V has completed
-      ok = ok && warp_wait(B.pv_done(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
-      ptx::tc_fence_after();
-      if (ok && !warp_aborted(sh) && ptx::elect_one()) {
-        const uint64_t dk = ptx::sdesc_sw128(sh.base + C::kOffK + s * C::kTileBytes, 16, 1024);
+    // QK^T of tile j, then P.V of tile j - 1 (its softmax overlaps QK^T(j));
+    // one more pass issues the last P.V
+    for (int j = 0; j <= T; ++j) {
+      if (j < T) {
+        const int s = (g + j) % C::kStages;
+        const int sb = (gm + j) & 1;
+        bool ok = qok && warp_wait(B.kfull(s), ((g + j) / C::kStages) & 1, sh, p.err, p.wait_timeout_ns);
+        // S buffer sb holds P of the tile two back until that P.V has completed
+        ok = ok && warp_wait(B.pv_done(sb), (((gm + j) >> 1) + 1) & 1, sh, p.err, p.wait_timeout_ns);
+        ptx::tc_fence_after();
+        if (ok && !warp_aborted(sh) && ptx::elect_one()) {
+          const uint64_t dk = ptx::sdesc_sw128(sh.base + C::kOffK + s * C::kTileBytes, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qoff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * (kTileTok * 128) + (kk & 3) * 32;
-          ptx::mma_bf16(tmem + sb * kTileTok, dq + (qoff >> 4), dk + (koff >> 4), C::kIdescQK,
-                        kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qoff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * (kTileTok * 128) + (kk & 3) * 32;
+            ptx::mma_bf16(tmem + sb * kTileTok, dq + (qoff >> 4), dk + (koff >> 4), C::kIdescQK,
+                          kk > 0 ? 1u : 0u);
+          }
+          issued = true;
         }
-        issued = true;
-      }
-      if (ptx::elect_one()) {
-        ptx::mma_commit(B.s_full(sb));
-        ptx::mma_commit(B.kempty(s));
+        if (ptx::elect_one()) {
+          ptx::mma_commit(B.s_full(sb));
+          ptx::mma_commit(B.kempty(s));
+        }
       }
       if (j > 0) issue_pv(j - 1);
     }
-    issue_pv(T - 1);
     if (ptx::elect_one()) ptx::mma_commit(B.o_full());
     g += T;
     gm += T;
@@ -840,6 +843,29 @@ __device__ __noinline__ void rescale_o(uint32_t o_tmem, float alpha) {
   ptx::tmem_wait_st();
 }
 
+// A unit whose span holds no page: each of its rows gets out = 0 and
+// lse = -inf (or that partial).  Rare, so out of line.
+template <int D>
+__device__ __noinline__ void empty_unit(const AttnParams& p, const UnitDesc& u, const Shared& sh) {
+  const int tid = threadIdx.x;
+  const GroupTok gt = tid < u.nrows ? p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa]
+                                    : GroupTok{-1, 0, -1, 0};
+  if (gt.tok < 0 || *sh.abort_flag) return;
+  const int h = unit_head(p, u, u.row0 + tid);
+  if (gt.pbase < 0) {
+    float* dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
+    if (p.lse) p.lse[(size_t)gt.tok * p.hq + h] = -INFINITY;
+    for (int c = 0; c < D; c += 4)
+      *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
+    uint16_t* dst = p.part_o + slot * D;
+    p.part_ml[slot] = make_float2(-INFINITY, 1.f);
+    for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+    if (p.merge_fused) merge_row_thread<D>(p, gt, h);
+  }
+}
+
 // The four compute warps: thread i owns TMEM lane / query row i.
 template <int D>
 __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared& sh,
@@ -869,24 +895,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     if (ui + 1 < u1) un = p.units[ui + 1];
     const int T = unit_tiles(u);
     if (T == 0) {  // empty span: every row sees nothing
-      const GroupTok gt = tid < u.nrows ? p.gtoks[u.tok_off + (u.row0 + tid) / p.gqa]
-                                        : GroupTok{-1, 0, -1, 0};
-      if (gt.tok >= 0 && !*sh.abort_flag) {
-        const int grow = u.row0 + tid;
-        const int h = unit_head(p, u, grow);
-        if (gt.pbase < 0) {
-          float* dst = p.out + ((size_t)gt.tok * p.hq + h) * D;
-          if (p.lse) p.lse[(size_t)gt.tok * p.hq + h] = -INFINITY;
-          for (int c = 0; c < D; c += 4)
-            *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          const size_t slot = (size_t)(gt.pbase + u.chunk) * p.hq + h;
-          uint16_t* dst = p.part_o + slot * D;
-          p.part_ml[slot] = make_float2(-INFINITY, 1.f);
-          for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
-        }
-        if (gt.pbase >= 0 && p.merge_fused) merge_row_thread<D>(p, gt, h);
-      }
+      empty_unit<D>(p, u, sh);
       continue;
     }
     if (!(u.path & kPathMma)) {
@@ -944,12 +953,6 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         bool ok = wait_bar(B.s_full(sb), ((gm + j) >> 1) & 1, sh, p.err, p.wait_timeout_ns);
         ok = __all_sync(0xffffffffu, ok);
         ptx::tc_fence_after();
-        // every QK^T of this unit has completed once the last S is ready: the
-        // query buffer is free, so the next unit's query tile starts streaming
-        if (j == T - 1 && nxt >= 0) {
-          load_q<D>(q_next, qbuf, tid);
-          gt_next = q_next.gt;
-        }
         float m_new = m_run, alpha = 1.f, lsum = 0.f;
         uint32_t pk[kTileTok / 2];
         // P rounds to bf16 for the tensor cores; the row sum is kept exact in
@@ -1064,9 +1067,13 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       tile_loop(std::true_type{});
     else
       tile_loop(std::false_type{});
-    // hand the next unit's query tile to the MMA issuer, so its first QK^T
-    // overlaps this unit's epilogue
+    // Every QK^T of this unit has completed (its last S was ready): the
+    // query buffer is free.  The next unit's query tile streams in while
+    // the last P.V runs and goes to the MMA issuer, so its first QK^T
+    // overlaps this unit's epilogue.
     if (nxt >= 0) {
+      load_q<D>(q_next, qbuf, tid);
+      gt_next = q_next.gt;
       ptx::cp_async_wait_all();
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(B.q_full(0));
