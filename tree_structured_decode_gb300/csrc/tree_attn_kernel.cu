@@ -304,6 +304,9 @@ __device__ void mma_issuer(const AttnParams& p, int u0, int u1, const Shared& sh
       continue;
     }
     const bool qok = warp_wait(B.q_full(0), nu & 1, sh, p.err, p.wait_timeout_ns);
+    // the query rows were written by the compute warps' cp.async (generic
+    // proxy); the tensor cores read them through the async proxy
+    ptx::fence_proxy_async_smem();
     ptx::tc_fence_after();
     const uint32_t o_tmem = tmem + 128;
     auto issue_pv = [&](int jj) {
@@ -755,7 +758,8 @@ __device__ __forceinline__ QRow q_row(const AttnParams& p, int k, int tid) {
 }
 
 // Start copying a query row into row tid of the swizzled buffer at qb (zeros
-// for a row without a token).  Completion: cp_async_wait_all().
+// for a row without a token).  Completion: cp_async_mbar_arrive_noinc() on
+// the buffer's barrier.
 template <int D>
 __device__ __forceinline__ void load_q(const QRow& r, uint32_t qb, int tid) {
   const uint32_t n = r.gt.tok >= 0 ? 16u : 0u;
@@ -884,9 +888,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       const QRow r = q_row<D>(p, first, tid);
       load_q<D>(r, qbuf, tid);
       gt_next = r.gt;
-      ptx::cp_async_wait_all();
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(B.q_full(0));
+      ptx::cp_async_mbar_arrive_noinc(B.q_full(0));
     }
   }
   UnitDesc un = u0 < u1 ? p.units[u0] : UnitDesc{};
@@ -1069,14 +1071,13 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       tile_loop(std::false_type{});
     // Every QK^T of this unit has completed (its last S was ready): the
     // query buffer is free.  The next unit's query tile streams in while
-    // the last P.V runs and goes to the MMA issuer, so its first QK^T
-    // overlaps this unit's epilogue.
+    // the last P.V runs; its copies arrive on q_full by themselves, so the
+    // compute warps go straight on to the epilogue and the next unit's first
+    // QK^T overlaps it.
     if (nxt >= 0) {
       load_q<D>(q_next, qbuf, tid);
       gt_next = q_next.gt;
-      ptx::cp_async_wait_all();
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(B.q_full(0));
+      ptx::cp_async_mbar_arrive_noinc(B.q_full(0));
     }
     // ---- epilogue: O / l, 32 columns at a time; then O is free again
     bool ok = wait_bar(B.o_full(), nu & 1, sh, p.err, p.wait_timeout_ns);
@@ -1116,6 +1117,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
     gm += T;
     ++nu;
   }
+  ptx::cp_async_wait_all();  // no copy of this thread is in flight when the CTA ends
 }
 
 template <int D>
