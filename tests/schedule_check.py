@@ -29,10 +29,10 @@ from __future__ import annotations
 
 import numpy as np
 
-PATH_MMA, PATH_HEADS, PATH_PHASES = 1, 2, 4
+PATH_MMA, PATH_HEADS, PATH_PHASES, PATH_PAIRS = 1, 2, 4, 16
 PHASE_SHIFT = 30
 POS_MASK = (1 << PHASE_SHIFT) - 1
-MMA_TILE_ROWS, SIMT_TILE_ROWS, SLOT_ROWS, BLOCKS_PER_TILE = 128, 8, 32, 4
+MMA_TILE_ROWS, SIMT_TILE_ROWS, SLOT_ROWS, PAIR_ROWS, BLOCKS_PER_TILE = 128, 8, 32, 64, 4
 
 
 def _key_tables(spec, seed=12345):
@@ -91,6 +91,8 @@ def unit_kind(u, rec_slot):
     tok_off, kvh, row0, nrows, b0, b1, chunk, path = (int(x) for x in u)
     if not path & PATH_MMA:
         return "simt"
+    if path & PATH_PAIRS:
+        return "pairs"
     if path & PATH_PHASES:
         return "packed_phases"
     if path & PATH_HEADS:
@@ -153,8 +155,11 @@ def check_schedule(spec, sched, num_sms=None, collect=False):
         live = tok >= 0
         if not live.any():
             continue
-        # q head of each row (a unit packed by kv head: 32-row slot k is kv head kvh + k)
-        head_kv = kvh + (grow // SLOT_ROWS if (mma and path & PATH_HEADS) else 0)
+        # q head of each row (a unit packed by kv head: 32-row slot k is kv head
+        # kvh + k; a pair unit: 64-row slot k)
+        pairs = bool(mma and path & PATH_PAIRS)
+        head_kv = kvh + (grow // SLOT_ROWS if (mma and path & PATH_HEADS)
+                         else grow // PAIR_ROWS if pairs else 0)
         head = head_kv * r + grow % r
         # blocks of the unit, tile by tile: page index bb inside its tile
         nb = b1 - b0
@@ -163,7 +168,13 @@ def check_schedule(spec, sched, num_sms=None, collect=False):
         page = blocks[b0:b1, 0]
         meta = blocks[b0:b1, 1]
         valid = meta & 31
-        if mma:
+        if mma and pairs:
+            # a pair unit: the rows of 64-row slot k see pages 2k, 2k + 1 of each tile
+            k = i // PAIR_ROWS
+            assert np.all(~live | (slot == k)), "pair row outside its slot"
+            see = (bb[None, :] // 2) == k[:, None]
+            pos = np.broadcast_to(meta[None, :] >> 5, (nr, nb))
+        elif mma:
             warp = i // 32
             packed = slot >= 0
             # a packed row reads page `warp` of each tile only; the planner
@@ -184,7 +195,7 @@ def check_schedule(spec, sched, num_sms=None, collect=False):
         lim = np.clip(np.minimum(valid[None, :], vis[:, None] - pos), 0, None)
         lim = np.where(see & live[:, None], lim, 0)
         # kv head whose K/V the block's page is loaded with
-        blk_kv = kvh + (bb if (mma and path & PATH_HEADS) else 0)
+        blk_kv = kvh + (bb if (mma and path & PATH_HEADS) else bb // 2 if pairs else 0)
         bkv = np.broadcast_to(blk_kv, (nb,)) if np.ndim(blk_kv) else np.full(nb, blk_kv)
         used = lim > 0
         if used.any():

@@ -58,12 +58,13 @@ def _stratified_tokens(spec, per_kind=4, n_random=24, seed=7, **options):
 
 def test_workload_parity_irregular_stratified():
     # the irregular tree: too many tokens for the oracle to check all of them,
-    # so the sample reaches every kind of unit the plan holds (full and
-    # half-filled 128-row tiles), rows masked inside a tile (the causal tail of
-    # the 4 speculative tokens, node ends) and every partial count
+    # so the sample reaches every kind of unit the plan holds (full 128-row
+    # tiles, the 64-row leaf tiles held by kv-head pairs), rows masked inside a
+    # tile (the causal tail of the 4 speculative tokens, node ends) and every
+    # partial count
     spec = W.config_irregular()
     toks, covered = _stratified_tokens(spec)
-    for kind in ("mma_full", "mma_half", "masked", "partials=1", "partials=2", "partials=3"):
+    for kind in ("mma_full", "pairs", "masked", "partials=1", "partials=2", "partials=3"):
         assert kind in covered, (kind, sorted(covered))
     q, k, v = make_inputs(spec, tail_fill=float("nan"))
     out, lse, stats = run_gpu(spec, q, k, v)
@@ -240,6 +241,33 @@ def test_packed_thin_groups(hq, hkv, path):
         out, lse, _ = run_gpu(spec, q, k, v, **opts)
         ref, ref_lse = oracle_on_tokens(spec, q, k, v, list(range(spec.n_queries)))
         compare(out, lse, ref, ref_lse)
+
+
+# ----------------------------------------------------------------- 64-row tiles in pairs
+@pytest.mark.parametrize("hq,hkv,ntok", [(64, 4, 4), (32, 8, 12), (16, 2, 7), (32, 4, 5)])
+@pytest.mark.parametrize("options", [{}, {"split_tokens": 96}, {"no_pack": 1}])
+def test_mid_size_tiles_held_by_kv_head_pairs(hq, hkv, ntok, options):
+    # leaves whose query tile holds 33-64 rows (ntok tokens x GQA), with page
+    # counts odd and even, under a root shared by all of them (whose larger
+    # group takes 128-row tiles plus a remainder tile): pair units (two kv
+    # heads per unit, two pages per slot per tile, a filler page for odd
+    # counts), or plain tiles with no_pack; every token against the oracle
+    rng = np.random.default_rng(hq + hkv + ntok)
+    nleaf = 6
+    lens = [333] + [int(x) for x in rng.integers(ntok, 260, size=nleaf)]
+    qnode = [v for v in range(1, nleaf + 1) for _ in range(ntok)]
+    qend = [lens[v] - ntok + 1 + j for v in range(1, nleaf + 1) for j in range(ntok)]
+    spec = W._finish("pairs", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=5)
+    toks, covered = _stratified_tokens(spec, **options)
+    if not options.get("no_pack"):
+        assert "pairs" in covered, sorted(covered)
+    else:
+        assert "pairs" not in covered
+    q, k, v = make_inputs(spec, tail_fill=float("nan"))
+    out, lse, _ = run_gpu(spec, q, k, v, **options)
+    toks = list(range(spec.n_queries))
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
+    compare(out, lse, ref, ref_lse, toks)
 
 
 # ----------------------------------------------------------------- kv-head packed units

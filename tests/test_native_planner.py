@@ -199,13 +199,16 @@ def test_schedule_check_catches_a_planted_fault():
     faults = []
     s1 = dict(sched)
     b = list(s1["blocks"])
-    i = next(k for k in range(1, len(b), 2) if b[k] & 31 > 1)
+    used = sorted({k for u in np.asarray(sched["units"]).reshape(-1, 8) for k in range(u[4], u[5])})
+    i = next(2 * k + 1 for k in used if b[2 * k + 1] & 31 > 1)  # a block some unit reads
     b[i] -= 1
     s1["blocks"] = b
     faults.append(s1)
     s2 = dict(sched)
     rows = list(s2["rows"])
-    j = next(k for k in range(0, len(rows), 4) if rows[k] >= 0 and rows[k + 3] & 0xFFFFFF == 1)
+    read = sorted({int(u[0]) + (int(u[2]) + i) // sched["gqa"]
+                   for u in np.asarray(sched["units"]).reshape(-1, 8) for i in range(min(int(u[3]), 128))})
+    j = next(4 * k for k in read if rows[4 * k] >= 0 and rows[4 * k + 3] & 0xFFFFFF == 1)  # a record some unit reads
     rows[j + 1] -= 1  # visible end one short
     s2["rows"] = rows
     faults.append(s2)

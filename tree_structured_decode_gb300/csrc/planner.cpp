@@ -413,6 +413,16 @@ tree_attn_status build_host_plan(
     if (k == kPathMma) (half_slot(p.groups[gi]) ? pack_mma2 : pack_mma).push_back((int32_t)gi);
     if (k == kPathSimt) pack_simt.push_back((int32_t)gi);
   }
+  // A tensor-core query tile of 33-64 rows runs as one slot of a pair unit
+  // (kUnitPairs): two kv heads of the group share the unit's 128 rows.
+  auto tile_rows = [&](const GroupInfo& g, int qt) {
+    return std::min(kMmaTileRows, g.rows - qt * kMmaTileRows);
+  };
+  auto pair_tile = [&](const GroupInfo& g, int qt) {
+    const int n = tile_rows(g, qt);
+    return !opt.no_pack && g.path == kPathMma && hkv % 2 == 0 && kPairRows % r == 0 &&
+           n > kPackMmaRows && n <= kPairRows;
+  };
   // Longer thin tensor-core groups are packed by kv head: four kv heads of
   // the group share a unit, slot k holding kv head kvh + k, and KV tile j
   // holds page j of the chunk once per slot.
@@ -422,6 +432,7 @@ tree_attn_status build_host_plan(
     for (int kvh = 0; kvh < hkv; ++kvh)
       for (int c = 0; c < g.nchunks; ++c)
         for (int qt = 0; qt < g.qtiles; ++qt) {
+          if (pair_tile(g, qt)) continue;  // emitted as a pair unit below
           UnitDesc u;
           u.tok_off = g.tok_off;
           u.kvh = kvh;
@@ -557,6 +568,57 @@ tree_attn_status build_host_plan(
         u.chunk = c;
         u.path = kPathMma | kUnitHeads;
         p.units.push_back(u);
+      }
+    }
+  }
+  // Pair units: row records slot by slot (the tile's rows for kv head kvh,
+  // then the same rows for kvh + 1; filler records past the tile's rows),
+  // shared by every chunk and head pair; per chunk a block list whose tile j
+  // holds pages 2j, 2j + 1 for the first head and again for the second (a
+  // zero-valid filler page when the chunk has an odd page count).
+  for (auto& g : p.groups) {
+    if (packable(g) >= 0 || head_thin(g)) continue;
+    for (int qt = 0; qt < g.qtiles; ++qt) {
+      if (!pair_tile(g, qt)) continue;
+      const int32_t tok_off = (int32_t)p.gtok.size();
+      const int t0 = qt * kMmaTileRows / r, nt = tile_rows(g, qt) / r;
+      for (int k = 0; k < 2; ++k)
+        for (int e = 0; e < kPairRows / r; ++e) {
+          if (e < nt) {
+            p.gtok.push_back(p.gtok[g.tok_off + t0 + e]);
+            p.gvis.push_back(p.gvis[g.tok_off + t0 + e]);
+            p.gpbase.push_back(p.gpbase[g.tok_off + t0 + e]);
+          } else {
+            p.gtok.push_back(-1);
+            p.gvis.push_back(0);
+            p.gpbase.push_back(-1);
+          }
+          p.gslot.push_back(k);
+        }
+      for (int c = 0; c < g.nchunks; ++c) {
+        const int32_t lo = p.chunk_lo[g.chunk_off + c], hi = p.chunk_hi[g.chunk_off + c];
+        const int32_t blk0 = (int32_t)p.blk_page.size();
+        for (int32_t b = lo; b < hi; b += 2)
+          for (int k = 0; k < 2; ++k) {
+            p.blk_page.push_back(p.blk_page[g.blk_off + b]);
+            p.blk_meta.push_back(p.blk_meta[g.blk_off + b]);
+            const bool second = b + 1 < hi;
+            p.blk_page.push_back(p.blk_page[g.blk_off + (second ? b + 1 : b)]);
+            p.blk_meta.push_back(second ? p.blk_meta[g.blk_off + b + 1] : 0);
+          }
+        const int32_t blk1 = (int32_t)p.blk_page.size();
+        for (int kvh = 0; kvh < hkv; kvh += 2) {
+          UnitDesc u;
+          u.tok_off = tok_off;
+          u.kvh = kvh;
+          u.row0 = 0;
+          u.nrows = 2 * kPairRows;
+          u.blk0 = blk0;
+          u.blk1 = blk1;
+          u.chunk = c;
+          u.path = kPathMma | kUnitPairs;
+          p.units.push_back(u);
+        }
       }
     }
   }

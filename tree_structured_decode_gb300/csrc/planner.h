@@ -38,6 +38,12 @@ constexpr int kUnitHeads = 2;  // with kPathMma: slot k of the unit is kv head k
 // groups of at most 16 rows, phase 0's in lanes 0-15 and phase 1's in lanes
 // 16-31, and the unit's tiles carry phase 0's pages, then phase 1's
 constexpr int kUnitPhases = 4;
+// with kPathMma: a query tile of 33-64 rows held once per kv head of a pair
+// (FastTree review page, 高效树结构注意力内核设计: smaller tiles near the
+// leaves): rows [64k, 64k + 64) are the tile for kv head kvh + k, and KV
+// tile j holds pages 2j and 2j + 1 of the chunk for each of the two heads
+constexpr int kUnitPairs = 16;
+constexpr int kPairRows = 64;
 constexpr int kPhasesMinUnitsPerCta = 3;         // two phases only with this many units per CTA
 constexpr int kPhaseShift = 30;                  // phase of a packed tile's page record
 constexpr int32_t kPosMask = (1 << kPhaseShift) - 1;

@@ -230,7 +230,9 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
       if (warp_aborted(sh)) continue;
       const bool leader = ptx::elect_one();
       if (leader) ptx::mbar_arrive_expect_tx(land, (uint32_t)nb * C::kBlockBytes);
-      const int kvh = u.kvh, hstep = (u.path & kUnitHeads) ? 1 : 0;  // page bb's kv head
+      // page bb's kv head: kvh + bb in a unit packed by kv head, kvh + bb / 2
+      // in a pair unit, else kvh
+      const int kvh = u.kvh, hsh = (u.path & kUnitHeads) ? 0 : (u.path & kUnitPairs) ? 1 : 3;
       const uint32_t dst = sh.base + (kIsV ? C::kOffV : C::kOffK) + s * C::kTileBytes;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
@@ -238,12 +240,12 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
           if constexpr (!kIsV) {
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h)
-              ptx::tma_load_4d(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0, kvh + bb * hstep,
+              ptx::tma_load_4d(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0, kvh + (bb >> hsh),
                                page[bb], land);
           } else if constexpr (D == 128) {  // both 64-column halves of V in one box
-            ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, kvh + bb * hstep, page[bb], land);
+            ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, kvh + (bb >> hsh), page[bb], land);
           } else {
-            ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, kvh + bb * hstep, page[bb], land);
+            ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, kvh + (bb >> hsh), page[bb], land);
           }
         }
       }
@@ -732,9 +734,10 @@ __device__ __forceinline__ int next_mma_unit(const AttnParams& p, int k, int u1)
 }
 
 // q head of row `row` (= row0 + tile row) of a unit; in a unit packed by kv
-// head, 32-row slot k belongs to kv head kvh + k.
+// head, 32-row slot k belongs to kv head kvh + k, in a pair unit 64-row slot k.
 __device__ __forceinline__ int unit_head(const AttnParams& p, const UnitDesc& u, int row) {
-  return (u.kvh + ((u.path & kUnitHeads) ? row / kPackMmaRows : 0)) * p.gqa + row % p.gqa;
+  const int slot = (u.path & kUnitHeads) ? row / kPackMmaRows : (u.path & kUnitPairs) ? row / kPairRows : 0;
+  return (u.kvh + slot) * p.gqa + row % p.gqa;
 }
 
 // Row tid of unit k's query tile: its record (token, visible end, partial
@@ -831,6 +834,43 @@ __device__ __noinline__ void rewrite_scaled_partial(const AttnParams& p, const U
   }
 }
 
+// One online-softmax step over N scores of this row (the ones it may not see
+// already -inf): the running max m_run is raised (to m_new, with the factor
+// alpha for what was summed before) only when the tile's max exceeds it by
+// more than 2^kRescaleLog2; P goes to pk as N / 2 bf16 pairs and the tile's
+// row sum of exponentials is returned (exact, in fp32).
+template <int N>
+__device__ __forceinline__ float softmax_step(const float (&sv)[N], float scale_log2, bool wact,
+                                              float m_run, float& m_new, float& alpha,
+                                              uint32_t* pk) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < N; c += 2) m4[(c >> 1) & 3] = ptx::max3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
+  const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
+  if (wact && mx > m_run + kRescaleLog2) {
+    m_new = mx;
+    alpha = ptx::ex2(m_run - m_new);
+  }
+  if (!wact) return 0.f;
+  // a row that has seen no key yet has only -inf scores here: any finite
+  // offset keeps their exponentials at 0 (and not NaN)
+  const float nm = m_new == -INFINITY ? 0.f : -m_new;
+  const uint64_t sc2 = ptx::f2(scale_log2, scale_log2), nm2 = ptx::f2(nm, nm);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // (0.f, 0.f) pairs
+#pragma unroll
+  for (int c = 0; c < N; c += 2) {
+    float xa, xb;
+    ptx::f2_split(ptx::fma_f32x2(ptx::f2(sv[c], sv[c + 1]), sc2, nm2), xa, xb);
+    const float a = ptx::ex2(xa), b = ptx::ex2(xb);
+    pk[c >> 1] = ptx::pack_bf16(a, b);
+    acc[(c >> 1) & 3] = ptx::add_f32x2(acc[(c >> 1) & 3], ptx::f2(a, b));
+  }
+  float e8[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) ptx::f2_split(acc[k], e8[2 * k], e8[2 * k + 1]);
+  return ((e8[0] + e8[1]) + (e8[2] + e8[3])) + ((e8[4] + e8[5]) + (e8[6] + e8[7]));
+}
+
 // O *= alpha for this thread's row (a lazy rescale: rare, so out of line,
 // which keeps the tile loop short)
 template <int D>
@@ -924,10 +964,14 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
       mt_p = packed ? __ldg(&blk[warp].y) : 0;
     };
     load_records(0);
-    // The tile loop in two forms, packed units' and the others', each
-    // compiled on its own: the loop a unit runs holds only its own form.
-    auto tile_loop = [&](auto packed_c) {
-      constexpr bool kPacked = decltype(packed_c)::value;
+    // The tile loop in three forms, each compiled on its own so that the
+    // loop a unit runs holds only its own: 0 a plain tile (64 columns per
+    // row), 1 a packed unit (a warp's 16 columns), 2 a pair unit (warps 2k,
+    // 2k + 1 hold kv head kvh + k and see S columns [32k, 32k + 32), pages
+    // 2k and 2k + 1 of every tile).
+    auto tile_loop = [&](auto form_c) {
+      constexpr int kForm = decltype(form_c)::value;
+      constexpr bool kPacked = kForm == 1;
       for (int j = 0; j < T; ++j) {
         const int sb = (gm + j) & 1;
         const int nb = min(kBpt, u.blk1 - (u.blk0 + kBpt * j));
@@ -985,6 +1029,22 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
             e4[(c >> 1) & 3] += a + b;
           }
           lsum = (e4[0] + e4[1]) + (e4[2] + e4[3]);
+        } else if constexpr (kForm == 2) {
+          const int sl = warp >> 1;
+          float sv[32];
+          if (ok && wact) {
+            ptx::tmem_ld32(tmem + lane_base + sb * kTileTok + sl * 32, sv);
+            ptx::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sv[c] = 0.f;
+          }
+          const int l0 = sl ? lim[2] : lim[0], l1 = sl ? lim[3] : lim[1];
+          if (!__all_sync(0xffffffffu, !row_ok || (l0 == 16 && l1 == 16))) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sv[c] = (c & 15) < (c < 16 ? l0 : l1) ? sv[c] : -INFINITY;
+          }
+          lsum = softmax_step<32>(sv, p.scale_log2, wact, m_run, m_new, alpha, pk);
         } else {
           float sv[kTileTok];
           if (ok && wact) {
@@ -1008,34 +1068,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 #pragma unroll
             for (int c = 0; c < kTileTok; ++c) sv[c] = (c & 15) < lim[c >> 4] ? sv[c] : -INFINITY;
           }
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int c = 0; c < kTileTok; c += 2)
-            m4[(c >> 1) & 3] = ptx::max3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
-          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
-          if (wact && mx > m_run + kRescaleLog2) {
-            m_new = mx;
-            alpha = ptx::ex2(m_run - m_new);
-          }
-          if (wact) {
-            // a row that has seen no key yet has only -inf scores here: any
-            // finite offset keeps their exponentials at 0 (and not NaN)
-            const float nm = m_new == -INFINITY ? 0.f : -m_new;
-            const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2), nm2 = ptx::f2(nm, nm);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // (0.f, 0.f) pairs
-#pragma unroll
-            for (int c = 0; c < kTileTok; c += 2) {
-              float xa, xb;
-              ptx::f2_split(ptx::fma_f32x2(ptx::f2(sv[c], sv[c + 1]), sc2, nm2), xa, xb);
-              const float a = ptx::ex2(xa), b = ptx::ex2(xb);
-              pk[c >> 1] = ptx::pack_bf16(a, b);
-              acc[(c >> 1) & 3] = ptx::add_f32x2(acc[(c >> 1) & 3], ptx::f2(a, b));
-            }
-            float e8[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) ptx::f2_split(acc[k], e8[2 * k], e8[2 * k + 1]);
-            lsum = ((e8[0] + e8[1]) + (e8[2] + e8[3])) + ((e8[4] + e8[5]) + (e8[6] + e8[7]));
-          }
+          lsum = softmax_step<kTileTok>(sv, p.scale_log2, wact, m_run, m_new, alpha, pk);
         }
         l_run = fmaf(l_run, alpha, lsum);
         m_run = m_new;
@@ -1056,6 +1089,13 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
 #pragma unroll
             for (int c = 0; c < kTileTok / 2; ++c) pw[c] = (c >> 3) == warp ? pk[c & 7] : 0u;
             ptx::tmem_st32u(pt, pw);
+          } else if constexpr (kForm == 2) {
+            // this slot's pages are P columns [16k, 16k + 16); the rest is zero
+            const int sl = warp >> 1;
+            uint32_t pw[kTileTok / 2];
+#pragma unroll
+            for (int c = 0; c < kTileTok / 2; ++c) pw[c] = (c >> 4) == sl ? pk[c & 15] : 0u;
+            ptx::tmem_st32u(pt, pw);
           } else {
             ptx::tmem_st32u(pt, pk);
           }
@@ -1065,10 +1105,12 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
         ptx::mbar_arrive(B.p_full(sb));
       }
     };
-    if (packed)
-      tile_loop(std::true_type{});
+    if (u.path & kUnitPairs)
+      tile_loop(std::integral_constant<int, 2>{});
+    else if (packed)
+      tile_loop(std::integral_constant<int, 1>{});
     else
-      tile_loop(std::false_type{});
+      tile_loop(std::integral_constant<int, 0>{});
     // Every QK^T of this unit has completed (its last S was ready): the
     // query buffer is free.  The next unit's query tile streams in while
     // the last P.V runs; its copies arrive on q_full by themselves, so the
