@@ -760,15 +760,27 @@ __device__ __forceinline__ QRow q_row(const AttnParams& p, int k, int tid) {
   return r;
 }
 
-// Start copying a query row into row tid of the swizzled buffer at qb (zeros
-// for a row without a token).  Completion: cp_async_mbar_arrive_noinc() on
-// the buffer's barrier.
+// Start copying the query rows into the swizzled buffer at qb (zeros for a
+// row without a token; thread tid looked up row tid).  Each warp copies its
+// own 32 rows a few at a time: lane l takes 16-byte chunk l % (d / 8) of
+// row l / (d / 8) of the group, so one instruction reads whole 256-byte rows
+// (d = 128: two rows) instead of one chunk of 32 scattered rows.
+// Completion: cp_async_mbar_arrive_noinc() on the buffer's barrier.
 template <int D>
 __device__ __forceinline__ void load_q(const QRow& r, uint32_t qb, int tid) {
-  const uint32_t n = r.gt.tok >= 0 ? 16u : 0u;
+  constexpr int kChunks = D / 8;          // 16-byte chunks per row
+  constexpr int kRows = 32 / kChunks;     // rows per instruction
+  const int lane = tid & 31, c = lane % kChunks;
+  const unsigned long long src = reinterpret_cast<unsigned long long>(r.src);
+  const int has = r.gt.tok >= 0;
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c)
-    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128(tid, c & 7), r.src + c * 8, n);
+  for (int k = 0; k < 32 / kRows; ++k) {
+    const int rr = k * kRows + lane / kChunks;  // row within the warp's 32
+    const unsigned long long s = __shfl_sync(0xffffffffu, src, rr);
+    const int h = __shfl_sync(0xffffffffu, has, rr);
+    ptx::cp_async16(qb + (c >> 3) * (128 * 128) + sw128((tid & ~31) + rr, c & 7),
+                    reinterpret_cast<const uint16_t*>(s) + c * 8, h ? 16u : 0u);
+  }
   ptx::cp_async_commit();
 }
 
