@@ -185,8 +185,10 @@ tree_attn_status tree_attn_plan(
  * Device pointers as in the conventions above; q, k_pages, v_pages are read,
  * out (and lse if non-NULL) written in full.  One plan may be run any number
  * of times (e.g. once per layer) but by one stream at a time: its workspace
- * is shared by all runs.  The current device must be the one the plan was
- * made on.  Errors: TA_ERR_INVALID_ARG (also: another device is current),
+ * is shared by all runs.  The runs of a decode step (one per layer) may be
+ * captured into one CUDA graph and replayed.  The current device must be
+ * the one the plan was made on.  Errors: TA_ERR_INVALID_ARG (also: another
+ * device is current),
  * TA_ERR_ALIGNMENT, TA_ERR_HOST_ONLY_PLAN, TA_ERR_CUDA (launch failure). */
 tree_attn_status tree_attn_run(tree_attn_plan_t plan, const void* q,
                                const void* k_pages, const void* v_pages,
@@ -233,8 +235,9 @@ tree_attn_status tree_attn_append_kv(tree_attn_plan_t plan, const void* k_new,
  *     stages that copy through its own buffer: the call returns once the
  *     copy is staged, and is not fully asynchronous to the host.
  *   - The first call on a device (and again after its context is made
- *     anew) looks up the scratch address on that device; make that first
- *     call before any stream capture.
+ *     anew) looks up the scratch address on that device.
+ *   - Its copy from pageable host memory is not for stream capture: run
+ *     this entry point outside a capture (tree_attn_run() captures).
  *   - Every call shares the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and corrupt each other's results.
  *     Serialise them, e.g. on one stream.
