@@ -7,8 +7,10 @@
 //
 //  * tensor cores (stacked query rows; FastTree review page, "高效树结构注意力
 //    内核设计": GEMV becomes GEMM once a group's queries are stacked): the
-//    group's query tile (128 rows = query tokens x GQA heads; or four thin
-//    groups packed one per warp) sits in shared memory; S = Q K^T goes to
+//    group's query tile (128 rows = query tokens x GQA heads; four thin
+//    groups, or four kv heads of one, packed one per warp; or a tile of at
+//    most 64 rows held once per kv head of a pair) sits in shared memory;
+//    S = Q K^T goes to
 //    TMEM (double-buffered), the four compute warps read one row per thread,
 //    apply the mask and an online softmax (the running max is raised only
 //    when it grows by more than 2^8, so O is rarely rescaled), write P as
@@ -24,8 +26,11 @@
 // notes page, "Tree-Topology-Aware Global Reduction Strategy").
 //
 // Roles: warps 0-3 compute (thread i owns TMEM lane / query row i), warp 4
-// streams K and warp 6 streams V by TMA, warp 5 owns TMEM and issues
-// tcgen05.mma; the issuing warps run converged, one elected lane issuing.
+// streams K and warp 6 streams V by TMA (and zeroes the V rows of unfilled
+// page slots), warp 5 owns TMEM and issues tcgen05.mma; the issuing warps
+// run converged, one elected lane issuing.  The compute warps' tile loop is
+// compiled once per unit form, and rare paths sit in out-of-line functions:
+// the speed of this kernel depends on how short its loops' code is.
 // Every wait is bounded: if one runs out the CTA records TA_DEVERR_TIMEOUT, stops issuing
 // work, waits (bounded) for its copies and MMAs in flight, frees TMEM and
 // returns.
