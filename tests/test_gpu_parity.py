@@ -244,9 +244,11 @@ def test_packed_thin_groups(hq, hkv, path):
 
 
 # ----------------------------------------------------------------- 64-row tiles in pairs
-@pytest.mark.parametrize("hq,hkv,ntok", [(64, 4, 4), (32, 8, 12), (16, 2, 7), (32, 4, 5)])
-@pytest.mark.parametrize("options", [{}, {"split_tokens": 96}, {"no_pack": 1}])
-def test_mid_size_tiles_held_by_kv_head_pairs(hq, hkv, ntok, options):
+@pytest.mark.parametrize("hq,hkv,ntok,d", [(64, 4, 4, 128), (32, 8, 12, 128), (16, 2, 7, 128),
+                                           (32, 4, 5, 128), (32, 4, 6, 64)])
+@pytest.mark.parametrize("options", [{}, {"split_tokens": 96}, {"no_pack": 1},
+                                     {"split_tokens": 96, "merge_mode": 1}])
+def test_mid_size_tiles_held_by_kv_head_pairs(hq, hkv, ntok, d, options):
     # leaves whose query tile holds 33-64 rows (ntok tokens x GQA), with page
     # counts odd and even, under a root shared by all of them (whose larger
     # group takes 128-row tiles plus a remainder tile): pair units (two kv
@@ -257,7 +259,7 @@ def test_mid_size_tiles_held_by_kv_head_pairs(hq, hkv, ntok, options):
     lens = [333] + [int(x) for x in rng.integers(ntok, 260, size=nleaf)]
     qnode = [v for v in range(1, nleaf + 1) for _ in range(ntok)]
     qend = [lens[v] - ntok + 1 + j for v in range(1, nleaf + 1) for j in range(ntok)]
-    spec = W._finish("pairs", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, 128, seed=5)
+    spec = W._finish("pairs", [-1] + [0] * nleaf, lens, qnode, qend, hq, hkv, d, seed=5)
     toks, covered = _stratified_tokens(spec, **options)
     if not options.get("no_pack"):
         assert "pairs" in covered, sorted(covered)

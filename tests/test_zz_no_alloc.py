@@ -39,7 +39,9 @@ def test_static_entry_point_matches_the_oracle_on_two_calls_in_a_row(merge_mode)
     import tree_structured_decode_gb300 as ta
 
     specs = [W.config_tiny(), W.random_tree(77, n_nodes=30, max_len=300, hq=8, hkv=2, d=128,
-                                            max_queries_per_node=3)]
+                                            max_queries_per_node=3),
+             # leaves of 4 tokens x GQA 16: 64-row tiles held by kv-head pairs
+             W.two_level(300, 6, 90, 64, 4, 128, seed=21, tokens_per_leaf=4)]
     data = [make_inputs(s, tail_fill=float("nan")) for s in specs]
     refs = [oracle_on_tokens(s, *d, list(range(s.n_queries))) for s, d in zip(specs, data)]
     plans = [ta.Plan.from_spec(s, host_only=1, split_tokens=128, merge_mode=merge_mode)
