@@ -167,6 +167,34 @@ def test_kv_head_packing_schedule(hq, hkv, ntok):
         _same(spec, **opt)
 
 
+@pytest.mark.parametrize("hq,hkv,ntok,pairs", [
+    (64, 4, 4, True),    # 64 rows (4 tokens x GQA 16): a pair slot
+    (32, 4, 5, True),    # 40 rows
+    (16, 2, 5, True),    # 40 rows, one kv-head pair
+    (64, 4, 5, False),   # 80 rows: a 128-row tile
+    (48, 3, 3, False),   # 48 rows but an odd kv-head count
+    (32, 4, 4, False),   # 32 rows: packed four to a unit instead
+    (128, 1, 1, False),  # GQA 128 does not divide a 64-row slot
+])
+def test_query_tiles_of_33_to_64_rows_form_kv_head_pairs(hq, hkv, ntok, pairs):
+    # the tile choice near the leaves (FastTree review page, 高效树结构注意力
+    # 内核设计): a leaf tile of 33-64 rows runs as one 64-row slot of a pair
+    # unit exactly when the kv heads pair up and the GQA ratio divides 64;
+    # the schedule stays valid either way
+    from schedule_check import check_schedule
+
+    rng = np.random.default_rng(hq + hkv + ntok)
+    lens = [500] + [int(x) for x in rng.integers(ntok, 300, size=5)]
+    qnode = [v for v in range(1, 6) for _ in range(ntok)]
+    qend = [lens[v] - (ntok - 1 - j) for v in range(1, 6) for j in range(ntok)]
+    spec = W._finish("tiles", [-1] + [0] * 5, lens, qnode, qend, hq, hkv, 128, seed=3)
+    for opt in ({}, {"split_tokens": 128}, {"no_pack": 1}):
+        _, _, sched = _native(spec, **opt)
+        facts = check_schedule(spec, sched, collect=True)
+        kinds = set().union(*facts["kinds"])
+        assert ("pairs" in kinds) == (pairs and not opt.get("no_pack")), (opt, sorted(kinds))
+
+
 @pytest.mark.parametrize("depth,branching,hq,hkv", [(3, 3, 32, 8), (2, 4, 64, 4), (4, 2, 8, 8)])
 def test_draft_token_trees_match_reference(depth, branching, hq, hkv):
     spec = W.token_tree(500, 4, 90, depth, branching, hq, hkv, 128, seed=depth)
