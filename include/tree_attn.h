@@ -283,11 +283,15 @@ tree_attn_status tree_attn_plan_describe(tree_attn_plan_t plan, char* buf,
 /* Canonical JSON of the tables the kernels of a run read, exactly as they
  * are copied to the device: the work units in schedule order (8 ints each:
  * first row record, kv head, first row, rows, first block, end block,
- * chunk, path flags), each CTA's unit range (cta_off), the blocks (page,
+ * chunk, path flags: 1 tensor cores, 2 slots are kv heads, 4 two phases,
+ * 16 a pair unit, 32 K/V no other unit reads), each CTA's unit range
+ * (cta_off), the blocks (page,
  * span position * 32 + valid slots, bit 30 the phase of a two-phase unit),
  * the row records (token, visible end, first partial slot, partial count |
  * (slot + 1) << 24), the merge items (token, first slot, count, 0) and each
- * token's first partial slot.  For tests and tools that check a schedule;
+ * token's first partial slot; kv_evict = 1 when the plan's K/V mostly
+ * streams once and its copies carry L2 policies.  For tests and tools that
+ * check a schedule;
  * same buffer rules as tree_attn_plan_describe(). */
 tree_attn_status tree_attn_plan_describe_schedule(tree_attn_plan_t plan, char* buf,
                                                   size_t cap, size_t* needed);

@@ -18,7 +18,10 @@ slot.  ``check_schedule`` decodes them the way the kernels do and asserts:
 * a unit reads the key of a page only through that page's own kv head
   (grouped-query attention: q head h reads kv head h // (Hq / Hkv));
 * the CTA ranges cover every unit exactly once and the merge items are the
-  tokens with two or more partials, with disjoint partial ranges.
+  tokens with two or more partials, with disjoint partial ranges;
+* a unit carries the read-once flag exactly when no other unit reads any
+  (page, kv head) it reads (zero-valid filler pages aside), and the plan
+  asks for L2 policies exactly when flagged units hold 3/4 of the tiles.
 
 Keys are compared as multisets through a count and a sum of random 64-bit
 hashes per (token, q head): a dropped, doubled or foreign key changes the sum
@@ -29,7 +32,7 @@ from __future__ import annotations
 
 import numpy as np
 
-PATH_MMA, PATH_HEADS, PATH_PHASES, PATH_PAIRS = 1, 2, 4, 16
+PATH_MMA, PATH_HEADS, PATH_PHASES, PATH_PAIRS, PATH_READ_ONCE = 1, 2, 4, 16, 32
 PHASE_SHIFT = 30
 POS_MASK = (1 << PHASE_SHIFT) - 1
 MMA_TILE_ROWS, SIMT_TILE_ROWS, SLOT_ROWS, PAIR_ROWS, BLOCKS_PER_TILE = 128, 8, 32, 64, 4
@@ -224,6 +227,35 @@ def check_schedule(spec, sched, num_sms=None, collect=False):
                 part_h[ps, h] += hsum[k]
                 assert part_tok[ps] in (-1, t)
                 part_tok[ps] = t
+
+    # ---- read-once flags: (page, kv head) pairs read by exactly one unit
+    def heads_of(u):
+        kvh, b0, b1, path = int(u[1]), int(u[4]), int(u[5]), int(u[7])
+        bb = np.arange(b1 - b0) % BLOCKS_PER_TILE
+        mma = bool(path & PATH_MMA)
+        if mma and path & PATH_HEADS:
+            return kvh + bb
+        if mma and path & PATH_PAIRS:
+            return kvh + bb // 2
+        return np.full(b1 - b0, kvh)
+    keys = []
+    for ui, u in enumerate(units):
+        b0, b1 = int(u[4]), int(u[5])
+        real = (blocks[b0:b1, 1] & 31) > 0
+        k = blocks[b0:b1, 0].astype(np.int64) * hkv + heads_of(u)
+        keys.append(k[real])
+    allk = np.concatenate(keys) if keys else np.zeros(0, np.int64)
+    uniq, counts = np.unique(allk, return_counts=True)
+    cnt_of = dict(zip(uniq.tolist(), counts.tolist()))
+    tiles = once_tiles = 0
+    for u, k in zip(units, keys):
+        once = int(u[5]) > int(u[4]) and all(cnt_of[int(x)] == 1 for x in k)
+        assert bool(int(u[7]) & PATH_READ_ONCE) == once, "read-once flag"
+        t = (int(u[5]) - int(u[4]) + BLOCKS_PER_TILE - 1) // BLOCKS_PER_TILE
+        tiles += t
+        once_tiles += t if once else 0
+    if "kv_evict" in sched:
+        assert bool(sched["kv_evict"]) == (tiles > 0 and 4 * once_tiles >= 3 * tiles), "kv_evict"
 
     # ---- merge items: tokens with >= 2 partials, disjoint slot ranges
     assert sorted(merge[:, 0].tolist()) == [t for t in range(nq) if pcount[t] >= 2]

@@ -76,9 +76,10 @@ struct MergeParams {
 };
 
 // Launch the persistent grouped partial-attention kernel (TMA + tcgen05 /
-// CUDA cores), one CTA per schedule entry.
+// CUDA cores), one CTA per schedule entry.  kv_evict: the plan's K/V mostly
+// streams once (HostPlan::kv_evict); its copies then carry L2 policies.
 cudaError_t launch_tree_attention(const AttnParams& p, int d, int grid, int num_pages,
-                                  cudaStream_t s);
+                                  bool kv_evict, cudaStream_t s);
 // Launch the log-sum-exp merge of partial results.
 cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s);
 // Copy each query token's new K and V (bf16 [nq][hkv][d]) into its page slot

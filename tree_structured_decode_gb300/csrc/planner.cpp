@@ -622,6 +622,32 @@ tree_attn_status build_host_plan(
       }
     }
   }
+  // Units whose K/V no other unit reads (counted per page and kv head; a
+  // pair unit's zero-valid filler pages do not count)
+  {
+    auto head_of = [&](const UnitDesc& u, int32_t b) {
+      const int bb = (b - u.blk0) % kBlocksPerTile;
+      return u.kvh + ((u.path & kUnitHeads) ? bb : (u.path & kUnitPairs) ? bb / 2 : 0);
+    };
+    std::vector<uint8_t> reads((size_t)num_pages * hkv, 0);
+    for (const UnitDesc& u : p.units)
+      for (int32_t b = u.blk0; b < u.blk1; ++b)
+        if (p.blk_meta[b] & 31) {
+          uint8_t& c = reads[(size_t)p.blk_page[b] * hkv + head_of(u, b)];
+          c = c < 2 ? c + 1 : 2;
+        }
+    int64_t tiles = 0, once_tiles = 0;
+    for (UnitDesc& u : p.units) {
+      bool once = true;
+      for (int32_t b = u.blk0; b < u.blk1 && once; ++b)
+        once = !(p.blk_meta[b] & 31) || reads[(size_t)p.blk_page[b] * hkv + head_of(u, b)] == 1;
+      if (once && u.blk1 > u.blk0) u.path |= kUnitReadOnce;
+      const int64_t t = ceil_div(u.blk1 - u.blk0, kBlocksPerTile);
+      tiles += t;
+      once_tiles += (u.path & kUnitReadOnce) ? t : 0;
+    }
+    p.kv_evict = tiles > 0 && 4 * once_tiles >= 3 * tiles;
+  }
   const int64_t nu = (int64_t)p.units.size();
   p.grid = (int32_t)std::min<int64_t>(nu, (int64_t)std::max(1, opt.num_sms) * kCtasPerSm);
   {

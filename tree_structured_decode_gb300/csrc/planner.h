@@ -44,6 +44,9 @@ constexpr int kUnitPhases = 4;
 // tile j holds pages 2j and 2j + 1 of the chunk for each of the two heads
 constexpr int kUnitPairs = 16;
 constexpr int kPairRows = 64;
+// every page (and kv head) the unit reads is read by no other unit: its K/V
+// copies ask L2 to evict those lines first
+constexpr int kUnitReadOnce = 32;
 constexpr int kPhasesMinUnitsPerCta = 3;         // two phases only with this many units per CTA
 constexpr int kPhaseShift = 30;                  // phase of a packed tile's page record
 constexpr int32_t kPosMask = (1 << kPhaseShift) - 1;
@@ -127,6 +130,11 @@ struct HostPlan {
   std::vector<UnitDesc> units;                // in schedule order (CTA-major)
   std::vector<int32_t> cta_off;               // CTA c runs units [cta_off[c], cta_off[c+1])
   int32_t grid = 0;
+  // the plan's K/V mostly streams once: at least 3/4 of its KV tiles are in
+  // units flagged kUnitReadOnce, and the kernel's copies carry L2 policies
+  // (evict-first for those units).  Measured: a plan that re-reads much of
+  // its K/V runs slower with the policies, one that streams it once faster.
+  bool kv_evict = false;
   // sizes
   int64_t unique_kv_tokens = 0, group_kv_tokens = 0, visible_pairs = 0;
 };

@@ -349,7 +349,7 @@ tree_attn_status tree_attn_run(tree_attn_plan_t P, const void* q, const void* k_
     e = cudaEventRecord(P->ev[0], s);
     if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord");
   }
-  e = ta::launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
+  e = ta::launch_tree_attention(ap, h.d, h.grid, h.num_pages, h.kv_evict, s);
   if (e != cudaSuccess) return cuda_err(e, "partial attention launch");
   if (P->profiling) {
     e = cudaEventRecord(P->ev[1], s);
@@ -476,7 +476,8 @@ tree_attn_status tree_attn_plan_describe_schedule(tree_attn_plan_t P, char* buf,
   s += "{\"hq\":" + std::to_string(h.hq) + ",\"hkv\":" + std::to_string(h.hkv) +
        ",\"gqa\":" + std::to_string(h.gqa) + ",\"d\":" + std::to_string(h.d) +
        ",\"grid\":" + std::to_string(h.grid) + ",\"n_partials\":" + std::to_string(h.n_partials) +
-       ",\"num_pages\":" + std::to_string(h.num_pages) + ",\"n_tokens\":" + std::to_string(h.nq);
+       ",\"num_pages\":" + std::to_string(h.num_pages) + ",\"n_tokens\":" + std::to_string(h.nq) +
+       ",\"kv_evict\":" + std::to_string(h.kv_evict ? 1 : 0);
   ints("units", img.off_units, img.n_units * sizeof(ta::UnitDesc) / 4);
   ints("cta_off", img.off_cta, img.n_cta);
   ints("blocks", img.off_blocks, img.n_blocks * 2);

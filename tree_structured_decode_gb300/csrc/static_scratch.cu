@@ -162,7 +162,7 @@ extern "C" tree_attn_status tree_attn_run_static(tree_attn_plan_t P, const void*
   ap.cta_inline = h.grid <= ta::kInlineCtas ? 1 : 0;
   if (ap.cta_inline)
     for (int c = 0; c <= h.grid; ++c) ap.cta_off_inline[c] = h.cta_off[c];
-  e = launch_tree_attention(ap, h.d, h.grid, h.num_pages, s);
+  e = launch_tree_attention(ap, h.d, h.grid, h.num_pages, h.kv_evict, s);
   if (e != cudaSuccess) return fail(TA_ERR_CUDA, std::string("partial attention launch: ") + cudaGetErrorString(e));
   if (img.n_merge && !ap.merge_fused) {
     MergeParams mp{};

@@ -194,7 +194,9 @@ __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x 
 // One warp streams K (kIsV false) or V (true) of every tile of the CTA's
 // units into the stage ring.  The whole warp runs the loop (its values stay
 // warp-uniform); one elected lane issues each copy.
-template <int D, bool kIsV>
+// kEvict (a plan whose K/V mostly streams once): each unit's copies carry an
+// L2 policy, evict-first for a unit whose K/V no other unit reads.
+template <int D, bool kIsV, bool kEvict>
 __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int u1,
                          const Shared& sh, const Bars<D>& B) {
   using C = Cfg<D>;
@@ -202,6 +204,13 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
   if (!kIsV && p.debug_stuck_wait) warp_wait(B.never(), 0, sh, p.err, p.wait_timeout_ns);
   uint32_t filled[C::kStages];  // 1 + tile index of the last fill issued per stage
   uint32_t land_par = 0;        // V: phase bit of each stage's vland barrier
+  // K/V that no other unit reads asks L2 to evict it first, leaving room to
+  // what is read again (shared spans, the partial results)
+  uint64_t pol_once = 0, pol_shared = 0;
+  if constexpr (kEvict) {
+    pol_once = ptx::policy_evict_first();
+    pol_shared = ptx::policy_evict_normal();
+  }
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) filled[s] = 0;
   UnitDesc un = u0 < u1 ? p.units[u0] : UnitDesc{};
@@ -238,6 +247,7 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
       // page bb's kv head: kvh + bb in a unit packed by kv head, kvh + bb / 2
       // in a pair unit, else kvh
       const int kvh = u.kvh, hsh = (u.path & kUnitHeads) ? 0 : (u.path & kUnitPairs) ? 1 : 3;
+      const uint64_t pol = (u.path & kUnitReadOnce) ? pol_once : pol_shared;
       const uint32_t dst = sh.base + (kIsV ? C::kOffV : C::kOffK) + s * C::kTileBytes;
 #pragma unroll
       for (int bb = 0; bb < kBpt; ++bb) {
@@ -245,12 +255,24 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
           if constexpr (!kIsV) {
 #pragma unroll
             for (int h = 0; h < C::kHalves; ++h)
-              ptx::tma_load_4d(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0, kvh + (bb >> hsh),
-                               page[bb], land);
+              if constexpr (kEvict)
+                ptx::tma_load_4d_hint(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0,
+                                      kvh + (bb >> hsh), page[bb], land, pol);
+              else
+                ptx::tma_load_4d(dst + h * (kTileTok * 128) + bb * 2048, tm, 64 * h, 0,
+                                 kvh + (bb >> hsh), page[bb], land);
           } else if constexpr (D == 128) {  // both 64-column halves of V in one box
-            ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, kvh + (bb >> hsh), page[bb], land);
+            if constexpr (kEvict)
+              ptx::tma_load_5d_hint(dst + bb * C::kBlockBytes, tm, 0, 0, 0, kvh + (bb >> hsh), page[bb],
+                                    land, pol);
+            else
+              ptx::tma_load_5d(dst + bb * C::kBlockBytes, tm, 0, 0, 0, kvh + (bb >> hsh), page[bb], land);
           } else {
-            ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, kvh + (bb >> hsh), page[bb], land);
+            if constexpr (kEvict)
+              ptx::tma_load_4d_hint(dst + bb * C::kBlockBytes, tm, 0, 0, kvh + (bb >> hsh), page[bb], land,
+                                    pol);
+            else
+              ptx::tma_load_4d(dst + bb * C::kBlockBytes, tm, 0, 0, kvh + (bb >> hsh), page[bb], land);
           }
         }
       }
@@ -1179,7 +1201,7 @@ __device__ void compute_warps(const AttnParams& p, int u0, int u1, const Shared&
   ptx::cp_async_wait_all();  // no copy of this thread is in flight when the CTA ends
 }
 
-template <int D>
+template <int D, bool kEvict>
 __global__ void __launch_bounds__(kThreads, 2)
     tree_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -1253,11 +1275,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else {
     ptx::setmaxnreg_dec<kIssueRegs>();
     if (warp == kProducerWarp) {
-      producer<D, false>(&tmk, p, u0, u1, sh, B);
+      producer<D, false, kEvict>(&tmk, p, u0, u1, sh, B);
     } else if (warp == kMmaWarp) {
       mma_issuer<D>(p, u0, u1, sh, B, tmem);
     } else if (warp == kVProducerWarp) {
-      producer<D, true>(&tmv, p, u0, u1, sh, B);
+      producer<D, true, kEvict>(&tmv, p, u0, u1, sh, B);
     }  // warp 7 only completes the warpgroup
     __syncwarp();
   }
@@ -1315,12 +1337,12 @@ cudaError_t make_page_map(CUtensorMap* m, const void* base, int d, int hkv, int 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, bool kEvict>
 cudaError_t launch_d(const AttnParams& p, int grid, int num_pages, cudaStream_t s) {
   // The shared-memory limit is an attribute of the kernel in the current
   // device's context: set on every launch (a host-side call of a few
   // microseconds), so a second device, or a context created anew, gets it too.
-  cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<D, kEvict>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   CUtensorMap mk, mv;
@@ -1332,16 +1354,19 @@ cudaError_t launch_d(const AttnParams& p, int grid, int num_pages, cudaStream_t 
     e = make_page_map(&mv, p.v, D, p.hkv, num_pages, true);
     if (e != cudaSuccess) return e;
   }
-  tree_attn_kernel<D><<<grid, kThreads, Cfg<D>::kSmem, s>>>(mk, mv, p);
+  tree_attn_kernel<D, kEvict><<<grid, kThreads, Cfg<D>::kSmem, s>>>(mk, mv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_tree_attention(const AttnParams& p, int d, int grid, int num_pages,
-                                  cudaStream_t s) {
+                                  bool kv_evict, cudaStream_t s) {
   if (p.n_units == 0 || grid == 0) return cudaSuccess;
-  return d == 128 ? launch_d<128>(p, grid, num_pages, s) : launch_d<64>(p, grid, num_pages, s);
+  if (d == 128)
+    return kv_evict ? launch_d<128, true>(p, grid, num_pages, s)
+                    : launch_d<128, false>(p, grid, num_pages, s);
+  return kv_evict ? launch_d<64, true>(p, grid, num_pages, s) : launch_d<64, false>(p, grid, num_pages, s);
 }
 
 }  // namespace ta
