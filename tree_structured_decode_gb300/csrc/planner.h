@@ -132,8 +132,9 @@ struct HostPlan {
   int32_t grid = 0;
   // the plan's K/V mostly streams once: at least 3/4 of its KV tiles are in
   // units flagged kUnitReadOnce, and the kernel's copies carry L2 policies
-  // (evict-first for those units).  Measured: a plan that re-reads much of
-  // its K/V runs slower with the policies, one that streams it once faster.
+  // (evict-first for those units, evict-last for the others).  Measured: a
+  // plan that re-reads much of its K/V runs slower with the policies, one
+  // that streams it once faster.
   bool kv_evict = false;
   // sizes
   int64_t unique_kv_tokens = 0, group_kv_tokens = 0, visible_pairs = 0;

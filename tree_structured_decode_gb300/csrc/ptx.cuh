@@ -127,15 +127,15 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, 
 }
 
 // L2 cache policies for bulk copies: evict the copied lines first (data no
-// other unit reads), or the normal priority.
+// other unit reads), or last (data read again).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-__device__ __forceinline__ uint64_t policy_evict_normal() {
+__device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 // tma_load_4d / tma_load_5d with an L2 cache policy

@@ -195,7 +195,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x 
 // units into the stage ring.  The whole warp runs the loop (its values stay
 // warp-uniform); one elected lane issues each copy.
 // kEvict (a plan whose K/V mostly streams once): each unit's copies carry an
-// L2 policy, evict-first for a unit whose K/V no other unit reads.
+// L2 policy, evict-first for a unit whose K/V no other unit reads, else
+// evict-last.
 template <int D, bool kIsV, bool kEvict>
 __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int u1,
                          const Shared& sh, const Bars<D>& B) {
@@ -204,12 +205,12 @@ __device__ void producer(const CUtensorMap* tm, const AttnParams& p, int u0, int
   if (!kIsV && p.debug_stuck_wait) warp_wait(B.never(), 0, sh, p.err, p.wait_timeout_ns);
   uint32_t filled[C::kStages];  // 1 + tile index of the last fill issued per stage
   uint32_t land_par = 0;        // V: phase bit of each stage's vland barrier
-  // K/V that no other unit reads asks L2 to evict it first, leaving room to
-  // what is read again (shared spans, the partial results)
+  // K/V that no other unit reads asks L2 to evict it first; K/V that other
+  // units read again asks to be evicted last
   uint64_t pol_once = 0, pol_shared = 0;
   if constexpr (kEvict) {
     pol_once = ptx::policy_evict_first();
-    pol_shared = ptx::policy_evict_normal();
+    pol_shared = ptx::policy_evict_last();
   }
 #pragma unroll
   for (int s = 0; s < C::kStages; ++s) filled[s] = 0;
