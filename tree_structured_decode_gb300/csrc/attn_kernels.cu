@@ -16,33 +16,36 @@ namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// Two (merge token, q head) rows per warp, 16 lanes each: a lane holds D / 16
-// columns (one 16-byte fp16 load per partial row for D = 128).  The partials
+// RPW (merge token, q head) rows per warp (two, or one for tokens with many
+// partials): a lane holds D * RPW / 32 columns (one 16- or 8-byte fp16 load
+// per partial row).  The partials
 // are read G at a time (lse and the lane's columns of G partial rows in
 // flight together, kept as packed fp16 until folded) and folded online: the
 // running max M only grows, and the sums kept so far are scaled by
 // 2^(M_old - M_new) when it does.  The launch picks G from the plan's
 // largest partial count (4, 8 or 24) so that a token takes one round of
 // loads where possible, with as few registers as that allows.
-template <int D, int G, int kMinBlocks>
+template <int D, int G, int kMinBlocks, int RPW = 2>
 __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeParams p) {
-  constexpr int EPL = D / 16;  // 8 or 4 columns per lane
-  constexpr int NW = EPL / 2;  // fp16 pairs per lane
-  const int lane = threadIdx.x & 31, sub = lane >> 4, l16 = lane & 15;
+  constexpr int LPR = 32 / RPW;  // lanes per row
+  constexpr int EPL = D / LPR;   // columns per lane
+  constexpr int NW = EPL / 2;    // fp16 pairs per lane
+  static_assert(EPL == 4 || EPL == 8, "a lane holds 4 or 8 columns");
+  const int lane = threadIdx.x & 31, sub = lane / LPR, l16 = lane % LPR;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int total = p.n_items * p.hq;
   // The merge items are plan tables, in place before the partial-attention
   // kernel started: this warp's first one is read before the dependency wait.
   MergeItem it_first = {};
-  if (2 * gw + sub < total) it_first = p.items[(2 * gw + sub) / p.hq];
+  if (RPW * gw + sub < total) it_first = p.items[(RPW * gw + sub) / p.hq];
   // launched as a programmatic dependent of the partial-attention kernel:
   // wait here until that grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int r0 = 2 * gw; r0 < total; r0 += 2 * nw) {
+  for (int r0 = RPW * gw; r0 < total; r0 += RPW * nw) {
     const int idx = r0 + sub;
     if (idx >= total) continue;
-    const MergeItem it = r0 == 2 * gw ? it_first : p.items[idx / p.hq];
+    const MergeItem it = r0 == RPW * gw ? it_first : p.items[idx / p.hq];
     const int h = idx % p.hq;
     const float2* ml_h = p.part_ml + (size_t)it.poff * p.hq + h;  // partial k at ml_h[k * hq]
     const uint16_t* o_h = p.part_o + ((size_t)it.poff * p.hq + h) * D + l16 * EPL;  // fp16
@@ -145,7 +148,10 @@ cudaError_t launch_append_kv(const uint16_t* k_new, const uint16_t* v_new, const
 
 cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
   if (p.n_items == 0) return cudaSuccess;
-  const long long warps = ((long long)p.n_items * p.hq + 1) / 2;  // two rows per warp
+  // two rows per warp, or one (each lane then holds 4 columns) when tokens
+  // have many partials: more warps share the same loads
+  const int rpw = (d == 128 && p.max_count > 8) ? 1 : 2;
+  const long long warps = ((long long)p.n_items * p.hq + rpw - 1) / rpw;
   const int blocks = (int)((warps + 7) / 8 < 152 * 16 ? (warps + 7) / 8 : 152 * 16);
   // A programmatic dependent launch: the merge grid may be scheduled while
   // the partial-attention kernel finishes (it waits in griddepcontrol.wait
@@ -163,7 +169,7 @@ cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
   // one round of loads per token where possible; fewer partials per round
   // leave registers for more resident warps
   if (d == 128) {
-    if (p.max_count > 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 24, 1>, p);
+    if (p.max_count > 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 24, 1, 1>, p);
     if (p.max_count > 4) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 8, 3>, p);
     return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 4, 5>, p);
   }
