@@ -109,6 +109,103 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
   }
 }
 
+// Tokens with at most G partials (one round of loads per row), software-
+// pipelined: a warp issues the loads of its next row before it folds the
+// current one, and the merge item of the row after that is read one row
+// further ahead, so that more loads are in flight per register.
+template <int D, int G, int kMinBlocks, int RPW = 2>
+__global__ void __launch_bounds__(256, kMinBlocks) lse_merge_pipelined_kernel(const MergeParams p) {
+  constexpr int LPR = 32 / RPW;
+  constexpr int EPL = D / LPR;
+  constexpr int NW = EPL / 2;
+  static_assert(EPL == 4 || EPL == 8, "a lane holds 4 or 8 columns");
+  const int lane = threadIdx.x & 31, sub = lane / LPR, l16 = lane % LPR;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int total = p.n_items * p.hq;
+  const int stride = RPW * nw;
+  int idx = RPW * gw + sub;
+  // plan tables, in place before the partial-attention kernel started
+  MergeItem it = {}, it_next = {};
+  if (idx < total) it = p.items[idx / p.hq];
+  if (idx + stride < total) it_next = p.items[(idx + stride) / p.hq];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  auto load = [&](int i, const MergeItem& m, float (&wq)[G], float (&oq)[G], uint32_t (&vq)[G][NW]) {
+    const int h = i % p.hq;
+    const float2* ml_h = p.part_ml + (size_t)m.poff * p.hq + h;
+    const uint16_t* o_h = p.part_o + ((size_t)m.poff * p.hq + h) * D + l16 * EPL;
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+      wq[q] = -INFINITY;
+      oq[q] = 1.f;
+#pragma unroll
+      for (int e = 0; e < NW; ++e) vq[q][e] = 0u;
+      if (i < total && q < m.count) {
+        const float2 ml = __ldcg(ml_h + (size_t)q * p.hq);
+        wq[q] = ml.x;
+        oq[q] = ml.y;
+        const uint16_t* src = o_h + (size_t)q * p.hq * D;
+        if constexpr (NW == 4) {
+          const uint4 t = __ldcg(reinterpret_cast<const uint4*>(src));
+          vq[q][0] = t.x, vq[q][1] = t.y, vq[q][2] = t.z, vq[q][3] = t.w;
+        } else {
+          const uint2 t = __ldcg(reinterpret_cast<const uint2*>(src));
+          vq[q][0] = t.x, vq[q][1] = t.y;
+        }
+      }
+    }
+  };
+  float w[G], osc[G];
+  uint32_t v[G][NW];
+  load(idx, it, w, osc, v);
+  for (; idx < total; idx += stride) {
+    // the next row's partials, and the item of the row after it
+    float w2[G], osc2[G];
+    uint32_t v2[G][NW];
+    load(idx + stride, it_next, w2, osc2, v2);
+    MergeItem it_after = {};
+    if (idx + 2 * stride < total) it_after = p.items[(idx + 2 * stride) / p.hq];
+    // fold this row: m = max lse_i, w_i = 2^(lse_i - m)
+    float m = w[0];
+#pragma unroll
+    for (int q = 1; q < G; ++q) m = fmaxf(m, w[q]);
+    float den = 0.f, acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        const float wq = exp2f(w[q] - m);  // 0 for absent or empty partials
+        den += wq;
+        const float wo = wq * osc[q];
+#pragma unroll
+        for (int e = 0; e < NW; ++e) {
+          const float2 f = ptx::unpack_f16(v[q][e]);
+          acc[2 * e] = fmaf(wo, f.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(wo, f.y, acc[2 * e + 1]);
+        }
+      }
+    }
+    const int h = idx % p.hq;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    float* dst = p.out + ((size_t)it.tok * p.hq + h) * D + l16 * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 4)
+      *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv);
+    if (l16 == 0 && p.lse)
+      p.lse[(size_t)it.tok * p.hq + h] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
+    it = it_next;
+    it_next = it_after;
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+      w[q] = w2[q];
+      osc[q] = osc2[q];
+#pragma unroll
+      for (int e = 0; e < NW; ++e) v[q][e] = v2[q][e];
+    }
+  }
+}
+
 // One thread per 16 bytes of a (token, kv head) row of K or V: the row of
 // token t, head h goes to page dst[t] / 16, slot dst[t] % 16, head h.
 __global__ void __launch_bounds__(256) append_kv_kernel(const uint4* k_new, const uint4* v_new,
@@ -167,11 +264,13 @@ cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // one round of loads per token where possible; fewer partials per round
-  // leave registers for more resident warps
+  // leave registers for more resident warps.  At d = 128, plans whose tokens
+  // have at most four partials take the software-pipelined form.
   if (d == 128) {
     if (p.max_count > 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 24, 1, 1>, p);
     if (p.max_count > 4) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 8, 3>, p);
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128, 4, 5>, p);
+    if (p.max_count > 3) return cudaLaunchKernelEx(&cfg, lse_merge_pipelined_kernel<128, 4, 3>, p);
+    return cudaLaunchKernelEx(&cfg, lse_merge_pipelined_kernel<128, 3, 4>, p);
   }
   if (p.max_count > 8) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<64, 24, 1>, p);
   if (p.max_count > 4) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<64, 8, 3>, p);
