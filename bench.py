@@ -339,6 +339,35 @@ def time_steps(plan, q, k, v, out, lse, flush, stream, steps, warmup, clocks=Non
     return step_ms, part_ms, merge_ms
 
 
+def time_layer_chain(plan, spec, dev, flush, stream, layers, iters=20, warmup=3):
+    """Per-layer time of `layers` back-to-back runs of the plan, each over
+    its own seeded Q and K/V pages (a decode step's layers), between one
+    event pair; L2 flushed before every chain.  Within a chain each run's
+    partial-attention kernel is a programmatic dependent of the previous
+    run's last kernel.  Returns (ms per layer, median over iters)."""
+    import torch
+
+    data = [W.make_tensors(spec, seed=1000 + i, device=dev) for i in range(layers)]
+    out = torch.empty((spec.n_queries, spec.n_q_heads, spec.head_dim), dtype=torch.float32,
+                      device=dev)
+    lse = torch.empty((spec.n_queries, spec.n_q_heads), dtype=torch.float32, device=dev)
+    res = []
+    for i in range(warmup + iters):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for q, k, v in data:
+            plan.run(q, k, v, out=out, lse=lse)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= warmup:
+            res.append(e0.elapsed_time(e1) / layers)
+    del data
+    torch.cuda.empty_cache()
+    return float(np.median(res))
+
+
 def roofline(work, t_part, t_step, workload):
     """The partial-attention kernel against the slower of the HBM and tensor
     bounds of the step's algorithmic bytes and FLOPs (measured peaks)."""
@@ -361,7 +390,7 @@ def roofline(work, t_part, t_step, workload):
     return roof
 
 
-def bench_workload(name, dev, flush, stream, steps, warmup, opts, clocks=None):
+def bench_workload(name, dev, flush, stream, steps, warmup, opts, clocks=None, chain_layers=0):
     """Plan and time one workload; returns its numbers and the live objects."""
     import torch
 
@@ -377,10 +406,19 @@ def bench_workload(name, dev, flush, stream, steps, warmup, opts, clocks=None):
     lse = torch.empty((spec.n_queries, spec.n_q_heads), dtype=torch.float32, device=dev)
     step_ms, part_ms, merge_ms = time_steps(plan, q, k, v, out, lse, flush, stream, steps, warmup,
                                             clocks)
+    chain_ms = (time_layer_chain(plan, spec, dev, flush, stream, chain_layers)
+                if chain_layers > 0 else None)
     code = plan.device_status()
     return {"spec": spec, "work": work, "plan": plan, "stats": stats, "q": q, "k": k, "v": v,
             "out": out, "lse": lse, "step_ms": step_ms, "part_ms": part_ms, "merge_ms": merge_ms,
-            "device_status": code}
+            "chain_ms": chain_ms, "device_status": code}
+
+
+def chain_record(work, chain_ms, layers):
+    if chain_ms is None:
+        return None
+    return {"layers": layers, "ms_per_layer": round(chain_ms, 5),
+            "gbs": round(work["bytes"] / (chain_ms * 1e-3) / 1e9, 1)}
 
 
 def bench_ours(args, rank, world, local):
@@ -401,7 +439,7 @@ def bench_ours(args, rank, world, local):
     torch.cuda.synchronize()
     clocks = NvmlClocks(dev)
     r = bench_workload(args.workload, dev, flush, stream, args.steps, args.warmup, opts,
-                       clocks if clocks.ok else None)
+                       clocks if clocks.ok else None, args.chain_layers)
     if world > 1:
         torch.distributed.barrier()
     spec, work, plan, stats = r["spec"], r["work"], r["plan"], r["stats"]
@@ -448,7 +486,8 @@ def bench_ours(args, rank, world, local):
         others = [n for n in ("tiny", "long", "wide", "three", "irreg") if n != args.workload]
         for name in others:
             rr = bench_workload(name, dev, flush, stream, args.per_workload_steps,
-                                min(args.warmup, 5), dict(args.plan_opts))
+                                min(args.warmup, 5), dict(args.plan_opts),
+                                chain_layers=args.chain_layers)
             ts = float(np.mean(rr["step_ms"]))
             tp = float(np.mean(rr["part_ms"]))
             rf = roofline(rr["work"], tp, ts, name)
@@ -460,7 +499,9 @@ def bench_ours(args, rank, world, local):
                          "kernel_frac": rf["frac"], "bound": rf["bound"],
                          "step_frac": rf["step_roofline_frac"], "traffic": rf["traffic"],
                          "alg_bytes_per_step": rr["work"]["bytes"],
-                         "n_units": rr["stats"]["n_units"], "device_status": rr["device_status"]}
+                         "n_units": rr["stats"]["n_units"],
+                         "layer_chain": chain_record(rr["work"], rr["chain_ms"], args.chain_layers),
+                         "device_status": rr["device_status"]}
             rr["plan"].close()
             del rr
             torch.cuda.empty_cache()
@@ -511,6 +552,7 @@ def bench_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
+        "layer_chain": chain_record(work, r["chain_ms"], args.chain_layers),
         "clocks": clocks.result() if clocks.ok else None,
         "device_status": r["device_status"],
         "per_workload": per,
@@ -632,6 +674,8 @@ def main():
     ap.add_argument("--per-workload-steps", type=int, default=20)
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--chain-layers", type=int, default=8,
+                    help="layers of the per-layer chain timing (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single-core-sample", default=None, help=argparse.SUPPRESS)

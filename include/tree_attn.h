@@ -186,7 +186,12 @@ tree_attn_status tree_attn_plan(
  * out (and lse if non-NULL) written in full.  One plan may be run any number
  * of times (e.g. once per layer) but by one stream at a time: its workspace
  * is shared by all runs.  The runs of a decode step (one per layer) may be
- * captured into one CUDA graph and replayed.  The current device must be
+ * captured into one CUDA graph and replayed.  The first kernel of a run is
+ * a programmatic dependent of the stream's previous kernel: its CTAs may be
+ * scheduled and set themselves up while that kernel finishes, but they read
+ * q, the pages and the plan's workspace, and write out and lse, only once
+ * that kernel has completed and its writes are visible (the usual stream
+ * order, for the data).  The current device must be
  * the one the plan was made on.  Errors: TA_ERR_INVALID_ARG (also: another
  * device is current),
  * TA_ERR_ALIGNMENT, TA_ERR_HOST_ONLY_PLAN, TA_ERR_CUDA (launch failure). */

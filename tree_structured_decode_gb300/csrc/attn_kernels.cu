@@ -42,6 +42,10 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
   // launched as a programmatic dependent of the partial-attention kernel:
   // wait here until that grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a small merge lets the stream's next kernel (a programmatic dependent, as
+  // the next partial-attention kernel is) be scheduled while it folds; a
+  // large one keeps the SMs to itself
+  if (p.early_trigger) asm volatile("griddepcontrol.launch_dependents;");
   for (int r0 = RPW * gw; r0 < total; r0 += RPW * nw) {
     const int idx = r0 + sub;
     if (idx >= total) continue;
@@ -130,6 +134,10 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_pipelined_kernel(co
   if (idx < total) it = p.items[idx / p.hq];
   if (idx + stride < total) it_next = p.items[(idx + stride) / p.hq];
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a small merge lets the stream's next kernel (a programmatic dependent, as
+  // the next partial-attention kernel is) be scheduled while it folds; a
+  // large one keeps the SMs to itself
+  if (p.early_trigger) asm volatile("griddepcontrol.launch_dependents;");
   auto load = [&](int i, const MergeItem& m, float (&wq)[G], float (&oq)[G], uint32_t (&vq)[G][NW]) {
     const int h = i % p.hq;
     const float2* ml_h = p.part_ml + (size_t)m.poff * p.hq + h;
@@ -243,8 +251,10 @@ cudaError_t launch_append_kv(const uint16_t* k_new, const uint16_t* v_new, const
   return cudaGetLastError();
 }
 
-cudaError_t launch_lse_merge(const MergeParams& p, int d, cudaStream_t s) {
-  if (p.n_items == 0) return cudaSuccess;
+cudaError_t launch_lse_merge(const MergeParams& params, int d, cudaStream_t s) {
+  if (params.n_items == 0) return cudaSuccess;
+  MergeParams p = params;
+  p.early_trigger = (int64_t)p.n_items * p.hq <= kMergeEarlyRows ? 1 : 0;
   // two rows per warp, or one (each lane then holds 4 columns) when tokens
   // have many partials: more warps share the same loads
   const int rpw = (d == 128 && p.max_count > 8) ? 1 : 2;

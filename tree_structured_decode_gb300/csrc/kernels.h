@@ -73,7 +73,11 @@ struct MergeParams {
   const float2* part_ml;     // {lse (log2 units), s}
   float* out;
   float* lse;
+  // at most kMergeEarlyRows (token, q head) rows: once the partials are
+  // visible the kernel lets the stream's next kernel be scheduled
+  int32_t early_trigger;
 };
+constexpr int64_t kMergeEarlyRows = 16384;
 
 // Launch the persistent grouped partial-attention kernel (TMA + tcgen05 /
 // CUDA cores), one CTA per schedule entry.  kv_evict: the plan's K/V mostly

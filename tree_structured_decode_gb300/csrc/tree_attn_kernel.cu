@@ -1269,6 +1269,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *sh.tmem_slot;
+  // This grid is launched as a programmatic dependent of the stream's
+  // previous kernel (often the previous layer's merge): the set-up above
+  // reads only this plan's tables, and the queries, pages, outputs and
+  // partials are touched only once that grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < kComputeThreads / 32) {
     ptx::setmaxnreg_inc<kComputeRegs>();
@@ -1355,8 +1360,19 @@ cudaError_t launch_d(const AttnParams& p, int grid, int num_pages, cudaStream_t 
     e = make_page_map(&mv, p.v, D, p.hkv, num_pages, true);
     if (e != cudaSuccess) return e;
   }
-  tree_attn_kernel<D, kEvict><<<grid, kThreads, Cfg<D>::kSmem, s>>>(mk, mv, p);
-  return cudaGetLastError();
+  // a programmatic dependent launch: the CTAs may be scheduled, and run their
+  // set-up, while the previous kernel in the stream finishes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tree_attn_kernel<D, kEvict>, mk, mv, p);
 }
 
 }  // namespace
