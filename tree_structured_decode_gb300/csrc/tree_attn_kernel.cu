@@ -52,16 +52,16 @@ namespace {
 // Two CTAs per SM, each a full pipeline of two warpgroups: four compute warps
 // (thread i owns TMEM lane / query row i) and one warpgroup holding the TMA
 // producer warps (K, V), the tcgen05 issuer warp and an idle warp.  The launch gives
-// every thread 128 registers; the roles rebalance to 192 (compute) and 64
-// (producer/issuer): 128 x 192 + 128 x 64 <= 256 x 128.  The second CTA on
+// every thread 128 registers; the roles rebalance to 200 (compute) and 56
+// (producer/issuer): 128 x 200 + 128 x 56 <= 256 x 128.  The second CTA on
 // the SM fills the latency gaps of the first.
 constexpr int kThreads = 256;
 constexpr int kComputeThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kVProducerWarp = 6;
-constexpr int kComputeRegs = 192;
-constexpr int kIssueRegs = 64;
+constexpr int kComputeRegs = 200;
+constexpr int kIssueRegs = 56;
 static_assert(128 * kComputeRegs + 128 * kIssueRegs <= kThreads * 128, "register split too large");
 constexpr int kTileTok = kKvTileTokens;  // KV tokens per tile (4 pages)
 constexpr int kBpt = kTileTok / 16;       // pages (blocks) per tile
