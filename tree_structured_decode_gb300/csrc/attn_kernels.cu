@@ -85,13 +85,13 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
       for (int q = 1; q < G; ++q) mr = fmaxf(mr, w[q]);
       const float m_new = fmaxf(M, mr);
       if (m_new == -INFINITY) continue;  // nothing visible so far
-      const float sc = exp2f(M - m_new);  // 0 while M is still -inf
+      const float sc = ptx::ex2(M - m_new);  // 0 while M is still -inf
       den *= sc;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] *= sc;
 #pragma unroll
       for (int q = 0; q < G; ++q) {
-        const float wq = exp2f(w[q] - m_new);  // 0 for absent or empty partials
+        const float wq = ptx::ex2(w[q] - m_new);  // 0 for absent or empty partials
         den += wq;
         const float wo = wq * osc[q];
 #pragma unroll
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_kernel(const MergeP
       }
       M = m_new;
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const float inv = den > 0.f ? __frcp_rn(den) : 0.f;
     float* dst = p.out + ((size_t)it.tok * p.hq + h) * D + l16 * EPL;
 #pragma unroll
     for (int e = 0; e < EPL; e += 4)
@@ -126,33 +126,48 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_pipelined_kernel(co
   const int lane = threadIdx.x & 31, sub = lane / LPR, l16 = lane % LPR;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
-  const int total = p.n_items * p.hq;
+  const int hq = p.hq;
+  // rows (item, q head) = divmod(RPW * gw + sub + k * stride, hq), k = 0, 1, ...:
+  // one division here, then an add and a carry per row
   const int stride = RPW * nw;
-  int idx = RPW * gw + sub;
+  const int s_item = stride / hq, s_h = stride % hq;
+  auto advance = [&](int& item, int& h) {
+    h += s_h;
+    item += s_item;
+    if (h >= hq) {
+      h -= hq;
+      ++item;
+    }
+  };
+  int item0 = (RPW * gw + sub) / hq, h0 = (RPW * gw + sub) % hq;  // this row
+  int item1 = item0, h1 = h0;
+  advance(item1, h1);  // the next
+  int item2 = item1, h2 = h1;
+  advance(item2, h2);  // the one after
   // plan tables, in place before the partial-attention kernel started
   MergeItem it = {}, it_next = {};
-  if (idx < total) it = p.items[idx / p.hq];
-  if (idx + stride < total) it_next = p.items[(idx + stride) / p.hq];
+  if (item0 < p.n_items) it = p.items[item0];
+  if (item1 < p.n_items) it_next = p.items[item1];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // a small merge lets the stream's next kernel (a programmatic dependent, as
   // the next partial-attention kernel is) be scheduled while it folds; a
   // large one keeps the SMs to itself
   if (p.early_trigger) asm volatile("griddepcontrol.launch_dependents;");
-  auto load = [&](int i, const MergeItem& m, float (&wq)[G], float (&oq)[G], uint32_t (&vq)[G][NW]) {
-    const int h = i % p.hq;
-    const float2* ml_h = p.part_ml + (size_t)m.poff * p.hq + h;
-    const uint16_t* o_h = p.part_o + ((size_t)m.poff * p.hq + h) * D + l16 * EPL;
+  auto load = [&](int item, int h, const MergeItem& m, float (&wq)[G], float (&oq)[G],
+                  uint32_t (&vq)[G][NW]) {
+    const float2* ml_h = p.part_ml + (size_t)m.poff * hq + h;
+    const uint16_t* o_h = p.part_o + ((size_t)m.poff * hq + h) * D + l16 * EPL;
 #pragma unroll
     for (int q = 0; q < G; ++q) {
       wq[q] = -INFINITY;
       oq[q] = 1.f;
 #pragma unroll
       for (int e = 0; e < NW; ++e) vq[q][e] = 0u;
-      if (i < total && q < m.count) {
-        const float2 ml = __ldcg(ml_h + (size_t)q * p.hq);
+      if (item < p.n_items && q < m.count) {
+        const float2 ml = __ldcg(ml_h + (size_t)q * hq);
         wq[q] = ml.x;
         oq[q] = ml.y;
-        const uint16_t* src = o_h + (size_t)q * p.hq * D;
+        const uint16_t* src = o_h + (size_t)q * hq * D;
         if constexpr (NW == 4) {
           const uint4 t = __ldcg(reinterpret_cast<const uint4*>(src));
           vq[q][0] = t.x, vq[q][1] = t.y, vq[q][2] = t.z, vq[q][3] = t.w;
@@ -165,14 +180,14 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_pipelined_kernel(co
   };
   float w[G], osc[G];
   uint32_t v[G][NW];
-  load(idx, it, w, osc, v);
-  for (; idx < total; idx += stride) {
+  load(item0, h0, it, w, osc, v);
+  while (item0 < p.n_items) {
     // the next row's partials, and the item of the row after it
     float w2[G], osc2[G];
     uint32_t v2[G][NW];
-    load(idx + stride, it_next, w2, osc2, v2);
+    load(item1, h1, it_next, w2, osc2, v2);
     MergeItem it_after = {};
-    if (idx + 2 * stride < total) it_after = p.items[(idx + 2 * stride) / p.hq];
+    if (item2 < p.n_items) it_after = p.items[item2];
     // fold this row: m = max lse_i, w_i = 2^(lse_i - m)
     float m = w[0];
 #pragma unroll
@@ -183,7 +198,7 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_pipelined_kernel(co
     if (m != -INFINITY) {
 #pragma unroll
       for (int q = 0; q < G; ++q) {
-        const float wq = exp2f(w[q] - m);  // 0 for absent or empty partials
+        const float wq = ptx::ex2(w[q] - m);  // 0 for absent or empty partials
         den += wq;
         const float wo = wq * osc[q];
 #pragma unroll
@@ -194,16 +209,18 @@ __global__ void __launch_bounds__(256, kMinBlocks) lse_merge_pipelined_kernel(co
         }
       }
     }
-    const int h = idx % p.hq;
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    float* dst = p.out + ((size_t)it.tok * p.hq + h) * D + l16 * EPL;
+    const float inv = den > 0.f ? __frcp_rn(den) : 0.f;
+    float* dst = p.out + ((size_t)it.tok * hq + h0) * D + l16 * EPL;
 #pragma unroll
     for (int e = 0; e < EPL; e += 4)
       *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e] * inv, acc[e + 1] * inv, acc[e + 2] * inv, acc[e + 3] * inv);
     if (l16 == 0 && p.lse)
-      p.lse[(size_t)it.tok * p.hq + h] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
+      p.lse[(size_t)it.tok * hq + h0] = den > 0.f ? (m + log2f(den)) * kLn2 : -INFINITY;
     it = it_next;
     it_next = it_after;
+    item0 = item1, h0 = h1;
+    item1 = item2, h1 = h2;
+    advance(item2, h2);
 #pragma unroll
     for (int q = 0; q < G; ++q) {
       w[q] = w2[q];
