@@ -191,7 +191,12 @@ tree_attn_status tree_attn_plan(
  * scheduled and set themselves up while that kernel finishes, but they read
  * q, the pages and the plan's workspace, and write out and lse, only once
  * that kernel has completed and its writes are visible (the usual stream
- * order, for the data).  The current device must be
+ * order, for the data).  A run's last kernel may in turn let the stream's
+ * next kernel be scheduled before it ends; a next kernel launched with
+ * programmatic stream serialization must therefore wait for its
+ * prerequisite grid (griddepcontrol.wait, cudaGridDependencySynchronize)
+ * before it reads out or lse, as such launches require anyway; any other
+ * launch sees the usual order.  The current device must be
  * the one the plan was made on.  Errors: TA_ERR_INVALID_ARG (also: another
  * device is current),
  * TA_ERR_ALIGNMENT, TA_ERR_HOST_ONLY_PLAN, TA_ERR_CUDA (launch failure). */
