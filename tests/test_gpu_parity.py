@@ -209,6 +209,20 @@ def test_fused_and_separate_merge(merge_mode):
     compare(out, lse, ref, ref_lse)
 
 
+def test_merge_rows_past_one_grid_stride():
+    # more merged (token, q head) rows than the merge grid covers in one
+    # stride, with Hq = 24 not dividing the stride: each warp's later rows
+    # come from the add-and-carry walk over (token, head)
+    spec = W.two_level(2000, 1800, 16, 24, 4, 128, seed=77)
+    q, k, v = make_inputs(spec)
+    out, lse, stats = run_gpu(spec, q, k, v)
+    assert stats["n_merge_tokens"] * spec.n_q_heads > 2 * 8 * 152 * 16
+    toks = sample_tokens(spec, 48, seed=3)
+    toks = sorted(set(toks) | set(range(spec.n_queries - 24, spec.n_queries)))
+    ref, ref_lse = oracle_on_tokens(spec, q, k, v, toks)
+    compare(out, lse, ref, ref_lse, toks)
+
+
 def test_fused_merge_counters_reset_between_runs():
     import tree_structured_decode_gb300 as ta
     spec = W.config_long()
