@@ -14,7 +14,10 @@ irregular random tree (depth 4-5, branching 1-8, node lengths log-uniform in
 16-2048, ~1000 leaves each carrying 4 speculative query tokens with a causal
 mask over its own last 4 tokens; 64 q / 4 kv heads, d = 128), bf16 N(0, 1)
 Q/K/V in 16-token pages in shuffled order.  The other four trees are timed
-the same way (fewer steps) and reported under "per_workload".
+the same way (fewer steps) and reported under "per_workload".  Beside the
+step: "layer_chain" (eight layers back to back, each its own Q and K/V),
+"append" (the step's K/V append, tree_attn_append_kv, timed alone) and
+"plan_ablation" (the headline tree under other plans and the fused merge).
 
 Metric: algorithmic HBM bytes per second (unique KV + Q + out + lse bytes of
 the step / device time of the step), with ms per step beside it.  Under
@@ -368,6 +371,36 @@ def time_layer_chain(plan, spec, dev, flush, stream, layers, iters=20, warmup=3)
     return float(np.median(res))
 
 
+def time_append(plan, spec, k, v, dev, flush, stream, steps, warmup=3):
+    """The decode step's K/V append (tree_attn_append_kv) for the workload's
+    query tokens, timed alone on copies of the page pools (L2 flushed before
+    each, one event pair around each).  Returns (median ms, bytes moved: the
+    new keys and values read and written once)."""
+    import torch
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    shape = (spec.n_queries, spec.n_kv_heads, spec.head_dim)
+    kn = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    vn = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    kk, vv = k.clone(), v.clone()
+    res = []
+    for i in range(warmup + steps):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        plan.append_kv(kn, vn, kk, vv)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= warmup:
+            res.append(e0.elapsed_time(e1))
+    nbytes = 2 * 2 * kn.numel() * kn.element_size()
+    del kk, vv, kn, vn
+    torch.cuda.empty_cache()
+    return float(np.median(res)), nbytes
+
+
 def roofline(work, t_part, t_step, workload):
     """The partial-attention kernel against the slower of the HBM and tensor
     bounds of the step's algorithmic bytes and FLOPs (measured peaks)."""
@@ -471,6 +504,9 @@ def bench_ours(args, rank, world, local):
             e2e_ms.append(e0.elapsed_time(e1))
     del dq, dk, dv, hq_, hk_, hv_
 
+    # ---- the step before the path: the new tokens' K/V into their pages
+    t_app, app_bytes = time_append(plan, spec, k, v, dev, flush, stream, args.per_workload_steps)
+
     t_step = float(np.mean(r["step_ms"]))
     t_part = float(np.mean(r["part_ms"]))
     t_merge = float(np.mean(r["merge_ms"]))
@@ -513,7 +549,8 @@ def bench_ours(args, rank, world, local):
     if not args.no_ablation and args.edges == "greedy" and not args.plan_opts:
         variants = (("greedy_latency_model", {}), ("greedy_pages_proxy", {"cost_model": 1}),
                     ("every_edge_0", {"force_edges": np.zeros(spec.n_nodes, dtype=np.int8)}),
-                    ("every_edge_1", {"force_edges": np.ones(spec.n_nodes, dtype=np.int8)}))
+                    ("every_edge_1", {"force_edges": np.ones(spec.n_nodes, dtype=np.int8)}),
+                    ("fused_merge", {"merge_mode": 1}))
         for name, opts2 in variants:
             rr = bench_workload(args.workload, dev, flush, stream, args.per_workload_steps,
                                 min(args.warmup, 5), opts2)
@@ -553,6 +590,8 @@ def bench_ours(args, rank, world, local):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
         "layer_chain": chain_record(work, r["chain_ms"], args.chain_layers),
+        "append": {"ms": round(t_app, 5), "bytes": app_bytes,
+                   "gbs": round(app_bytes / (t_app * 1e-3) / 1e9, 1)},
         "clocks": clocks.result() if clocks.ok else None,
         "device_status": r["device_status"],
         "per_workload": per,
